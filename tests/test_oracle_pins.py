@@ -1,0 +1,332 @@
+"""Pins of the fp64 oracle to facts other than itself (CPU only).
+
+Each test ties one part of the oracle to a closed form worked by hand, a
+library routine, an invariant, a special case, brute force on tiny inputs or
+a number the pages print. Together they are chosen so that a dropped term, a
+sign error, a wrong index or a transposed operand anywhere in the oracle
+fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import mla_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------- storage formats
+
+def test_bf16_rounding_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000).astype(np.float32),
+                        (rng.standard_normal(2000) * 1e-30).astype(np.float32),
+                        (rng.standard_normal(2000) * 1e30).astype(np.float32),
+                        np.array([1 + 2**-8, 1 + 3 * 2**-8, -(1 + 2**-8), 2**-130, 0.0],
+                                 dtype=np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x.astype(np.float64)), ref)
+
+
+def test_bf16_ties_to_even_by_hand():
+    # spacing of bf16 just above 1 is 2^-7; halfway points go to the even mantissa
+    assert O.round_to_bf16(np.array([1 + 2**-8]))[0] == 1.0
+    assert O.round_to_bf16(np.array([1 + 3 * 2**-8]))[0] == 1 + 2**-6
+    assert O.round_to_bf16(np.array([1 + 2**-8 + 2**-20]))[0] == 1 + 2**-7
+
+
+def test_e4m3_matches_torch_in_range():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.standard_normal(20000),
+                        rng.standard_normal(2000) * 2**-8]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_to_e4m3(x.astype(np.float64)), ref)
+
+
+def test_e4m3_by_hand():
+    v = O.round_to_e4m3(np.array([448.0, 500.0, -1e6, 2.0**-9, 2.0**-10, 1.0625, 1.1875, 240.0, 232.0]))
+    # max finite 448; saturation; smallest subnormal 2^-9; half of it ties to 0;
+    # 1.0625 ties to 1.0 (even); 1.1875 ties to 1.25 (even); 240 exact; 232 ties to 224 (even)
+    np.testing.assert_array_equal(v, [448.0, 448.0, -448.0, 2.0**-9, 0.0, 1.0, 1.25, 240.0, 224.0])
+
+
+def test_e4m3_block_quantisation_properties():
+    rng = np.random.default_rng(2)
+    c = rng.standard_normal((7, 256))
+    c[3, 128:] = 0.0                     # an all-zero block takes scale 1
+    codes, scales, deq = O.quantize_e4m3_blocks(c, 128)
+    assert scales.dtype == np.float32 and scales.shape == (7, 2)
+    assert scales[3, 1] == 1.0 and np.all(codes[3, 128:] == 0)
+    # every block's largest magnitude lands on (or within rounding of) +-448
+    amax_codes = np.abs(codes).reshape(7, 2, 128).max(axis=2)
+    assert np.all((amax_codes[[i for i in range(7)], 0] >= 416) & (amax_codes[:, 0] <= 448))
+    # dequantised error stays within half an E4M3 step (relative 2^-4) of each value
+    err = np.abs(deq - c)
+    s = np.repeat(scales.astype(np.float64), 128, axis=1)
+    assert np.all(err <= np.maximum(np.abs(c) * 2.0**-4, s * 2.0**-10) * 1.0001)
+
+
+# --------------------------------------------------------------- RMSNorm, RoPE
+
+def test_rmsnorm_by_hand_and_invariants():
+    eps = 1e-6
+    y = O.rmsnorm(np.array([3.0, 4.0]), eps)
+    np.testing.assert_allclose(y, np.array([3.0, 4.0]) / math.sqrt(12.5 + eps), rtol=0, atol=1e-15)
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 512))
+    y = O.rmsnorm(x, eps)
+    ms = np.mean(x * x, axis=1)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), 1 / np.sqrt(1 + eps / ms), rtol=1e-13)
+    np.testing.assert_allclose(O.rmsnorm(7.5 * x, 0.0), O.rmsnorm(x, 0.0), rtol=1e-13)
+    g = rng.standard_normal(512)
+    np.testing.assert_allclose(O.rmsnorm(x, eps, g), O.rmsnorm(x, eps) * g, rtol=1e-14)
+
+
+def test_rope_pairing_and_sign_by_hand():
+    d, theta = 8, 10000.0
+    for m in range(d // 2):
+        for pos in (0, 1, 37, 131071):
+            ang = pos * theta ** (-2.0 * m / d)
+            e = np.zeros(d)
+            e[2 * m] = 1.0
+            want = np.zeros(d)
+            want[2 * m], want[2 * m + 1] = math.cos(ang), math.sin(ang)
+            np.testing.assert_allclose(O.rope(e, pos, theta), want, atol=1e-12)
+            e = np.zeros(d)
+            e[2 * m + 1] = 1.0
+            want = np.zeros(d)
+            want[2 * m], want[2 * m + 1] = -math.sin(ang), math.cos(ang)
+            np.testing.assert_allclose(O.rope(e, pos, theta), want, atol=1e-12)
+            # half-split pairing: (m, m + d/2)
+            e = np.zeros(d)
+            e[m] = 1.0
+            want = np.zeros(d)
+            want[m], want[m + d // 2] = math.cos(ang), math.sin(ang)
+            np.testing.assert_allclose(O.rope(e, pos, theta, interleaved=False), want, atol=1e-12)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    np.testing.assert_array_equal(O.rope(q, 0, 1e4), q)
+    np.testing.assert_allclose(np.linalg.norm(O.rope(q, 12345, 1e4)), np.linalg.norm(q), rtol=1e-13)
+    for m, n, s in ((3, 9, 100), (1000, 17, 4096), (0, 0, 65000)):
+        a = O.rope(q, m, 1e4) @ O.rope(k, n, 1e4)
+        b = O.rope(q, m + s, 1e4) @ O.rope(k, n + s, 1e4)
+        assert abs(a - b) < 1e-9 * (1 + abs(a))
+
+
+# --------------------------------------------------------------- softmax, decode
+
+def test_softmax_matches_scipy_and_sums_to_one():
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((6, 300)) * 30
+    p = O.softmax_probs(z)
+    np.testing.assert_allclose(p, scipy.special.softmax(z, axis=1), rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.all(p >= 0)
+
+
+def _two_token_case():
+    """A decode worked by hand: one head, d_h=2, d_c=3, d_r=2, two cached tokens."""
+    eps, theta, scale = 1e-6, 10000.0, 0.7
+    c_raw = np.array([[3.0, 4.0, 0.0], [1.0, -1.0, 2.0]])
+    k_raw = np.array([[1.0, 0.0], [0.5, 2.0]])
+    w_uk = np.array([[1.0, 2.0, 0.0], [0.0, 1.0, -1.0]])     # [d_h, d_c]
+    w_uv = np.array([[1.0, 2.0, 3.0], [0.0, 1.0, -2.0]])     # [d_h, d_c]
+    q_nope = np.array([1.0, -1.0])
+    q_rope = np.array([0.3, -0.8])
+    # by hand: c_j = c_raw_j / sqrt(mean(c_raw_j^2) + eps)
+    n0, n1 = math.sqrt(25 / 3 + eps), math.sqrt(6 / 3 + eps)
+    c0, c1 = np.array([3, 4, 0]) / n0, np.array([1, -1, 2]) / n1
+    # d_r = 2: one pair at frequency 1, angle = position; token 0 unrotated
+    kr0 = np.array([1.0, 0.0])
+    a = 1.0
+    kr1 = np.array([0.5 * math.cos(a) - 2.0 * math.sin(a), 0.5 * math.sin(a) + 2.0 * math.cos(a)])
+    # k_{j} = [W_UK c_j ; kR_j]: W_UK c = (c[0] + 2 c[1], c[1] - c[2]); q_nope . that = c[0] + c[1] + c[2]
+    s0 = scale * ((c0[0] + c0[1] + c0[2]) + 0.3 * kr0[0] - 0.8 * kr0[1])
+    s1 = scale * ((c1[0] + c1[1] + c1[2]) + 0.3 * kr1[0] - 0.8 * kr1[1])
+    p1 = 1.0 / (1.0 + math.exp(s0 - s1))
+    p0 = 1.0 - p1
+    mix = p0 * c0 + p1 * c1
+    want = np.array([mix[0] + 2 * mix[1] + 3 * mix[2], mix[1] - 2 * mix[2]])
+    return dict(eps=eps, theta=theta, scale=scale, c_raw=c_raw, k_raw=k_raw, w_uk=w_uk,
+                w_uv=w_uv, q_nope=q_nope, q_rope=q_rope, want=want, p=np.array([p0, p1]))
+
+
+@pytest.mark.parametrize("form", ["explicit", "absorbed"])
+def test_two_token_decode_by_hand(form):
+    t = _two_token_case()
+    c = O.rmsnorm(t["c_raw"], t["eps"])
+    kr = O.rope(t["k_raw"], np.array([0, 1]), t["theta"])
+    fn = O.head_explicit if form == "explicit" else O.head_absorbed
+    out, p = fn(t["q_nope"], t["q_rope"], t["w_uk"], t["w_uv"], c, kr, t["scale"])
+    np.testing.assert_allclose(p, t["p"], rtol=1e-13)
+    np.testing.assert_allclose(out, t["want"], rtol=1e-13)
+
+
+def test_two_token_decode_catches_transposes_and_dropped_terms():
+    t = _two_token_case()
+    c = O.rmsnorm(t["c_raw"], t["eps"])
+    kr = O.rope(t["k_raw"], np.array([0, 1]), t["theta"])
+    base = t["want"]
+    # each plausible mistake moves the answer well away from the hand value
+    mistakes = [
+        dict(kr=np.zeros_like(kr)),                       # rope term dropped
+        dict(kr=O.rope(t["k_raw"], np.array([0, -1]), t["theta"])),   # rotation sign
+        dict(kr=O.rope(t["k_raw"], np.array([1, 2]), t["theta"])),    # 1-based positions
+        dict(scale=1.0),                                   # scale dropped
+        dict(w_uv=np.concatenate([t["w_uv"][:, ::-1]], axis=1)),      # reversed latent index
+    ]
+    for m in mistakes:
+        args = dict(q_nope=t["q_nope"], q_rope=t["q_rope"], w_uk=t["w_uk"], w_uv=t["w_uv"],
+                    c=c, kr=kr, scale=t["scale"])
+        args.update(m)
+        out, _ = O.head_explicit(args["q_nope"], args["q_rope"], args["w_uk"], args["w_uv"],
+                                 args["c"], args["kr"], args["scale"])
+        assert np.max(np.abs(out - base)) > 1e-3
+
+
+def _brute_force_mha(q_nope, q_rope, w_uk, w_uv, c, kr, scale):
+    """Textbook multi-head attention with keys/values built element by element."""
+    H, d_h, d_c = len(w_uk), len(w_uk[0]), len(w_uk[0][0])
+    L, d_r = len(kr), len(kr[0])
+    out = [[0.0] * d_h for _ in range(H)]
+    for i in range(H):
+        keys, vals = [], []
+        for j in range(L):
+            k = [sum(w_uk[i][r][s] * c[j][s] for s in range(d_c)) for r in range(d_h)]
+            k += [kr[j][r] for r in range(d_r)]
+            v = [sum(w_uv[i][r][s] * c[j][s] for s in range(d_c)) for r in range(d_h)]
+            keys.append(k)
+            vals.append(v)
+        q = list(q_nope[i]) + list(q_rope[i])
+        logits = [scale * sum(q[r] * keys[j][r] for r in range(d_h + d_r)) for j in range(L)]
+        mx = max(logits)
+        w = [math.exp(z - mx) for z in logits]
+        tot = sum(w)
+        for r in range(d_h):
+            out[i][r] = sum(w[j] * vals[j][r] for j in range(L)) / tot
+    return np.array(out)
+
+
+def test_oracle_equals_brute_force_mha_tiny():
+    rng = np.random.default_rng(6)
+    H, d_h, d_c, d_r, L = 3, 4, 5, 2, 7
+    q_nope, q_rope = rng.standard_normal((1, H, d_h)), rng.standard_normal((1, H, d_r))
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    c, kr = rng.standard_normal((L, d_c)), rng.standard_normal((L, d_r))
+    want = _brute_force_mha(q_nope[0].tolist(), q_rope[0].tolist(), w_uk.tolist(), w_uv.tolist(),
+                            c.tolist(), kr.tolist(), 0.37)
+    for form in ("explicit", "absorbed"):
+        got = O.decode(q_nope, q_rope, w_uk, w_uv, [c], [kr], 0.37, form=form)[0]
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_absorbed_equals_explicit_random_shapes():
+    rng = np.random.default_rng(7)
+    for (B, H, d_h, d_c, d_r) in ((2, 4, 16, 32, 8), (3, 5, 7, 11, 4), (1, 2, 128, 512, 64)):
+        lens = rng.integers(1, 40, size=B)
+        q_nope, q_rope = rng.standard_normal((B, H, d_h)), rng.standard_normal((B, H, d_r))
+        w_uk, w_uv = rng.standard_normal((H, d_h, d_c)) * 0.2, rng.standard_normal((H, d_h, d_c)) * 0.2
+        cs = [rng.standard_normal((n, d_c)) for n in lens]
+        krs = [rng.standard_normal((n, d_r)) for n in lens]
+        a = O.decode(q_nope, q_rope, w_uk, w_uv, cs, krs, 0.2, form="absorbed")
+        e = O.decode(q_nope, q_rope, w_uk, w_uv, cs, krs, 0.2, form="explicit")
+        assert np.max(np.abs(a - e)) <= 1e-10 * np.max(np.abs(e))
+
+
+def test_special_cases():
+    rng = np.random.default_rng(8)
+    H, d_h, d_c, d_r = 3, 6, 10, 4
+    q_nope, q_rope = rng.standard_normal((1, H, d_h)), rng.standard_normal((1, H, d_r))
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    # one cached token: attention returns its value exactly
+    c1, kr1 = rng.standard_normal((1, d_c)), rng.standard_normal((1, d_r))
+    out = O.decode(q_nope, q_rope, w_uk, w_uv, [c1], [kr1], 0.5)
+    for i in range(H):
+        np.testing.assert_allclose(out[0, i], w_uv[i] @ c1[0], rtol=1e-13)
+    # identical rows: uniform weights, value of the row
+    c, kr = np.repeat(c1, 9, axis=0), np.repeat(kr1, 9, axis=0)
+    out = O.decode(q_nope, q_rope, w_uk, w_uv, [c], [kr], 0.5, form="explicit")
+    for i in range(H):
+        np.testing.assert_allclose(out[0, i], w_uv[i] @ c1[0], rtol=1e-12)
+    # no key signal at all: plain mean of the values
+    c, kr = rng.standard_normal((9, d_c)), rng.standard_normal((9, d_r))
+    out = O.decode(q_nope, np.zeros_like(q_rope), np.zeros_like(w_uk), w_uv, [c], [kr], 0.5)
+    for i in range(H):
+        np.testing.assert_allclose(out[0, i], w_uv[i] @ c.mean(axis=0), rtol=1e-12)
+    # empty cache gives zeros; a zeroed head gives zeros only for that head
+    out = O.decode(q_nope, q_rope, w_uk, w_uv, [np.zeros((0, d_c))], [np.zeros((0, d_r))], 0.5)
+    assert np.all(out == 0)
+    w0 = w_uv.copy()
+    w0[1] = 0
+    out = O.decode(q_nope, q_rope, w_uk, w0, [c], [kr], 0.5)
+    assert np.all(out[0, 1] == 0) and np.all(np.abs(out[0, 0]) > 0)
+
+
+def test_probs_sum_to_one_on_long_sequence():
+    rng = np.random.default_rng(9)
+    c, kr = rng.standard_normal((5000, 32)), rng.standard_normal((5000, 8))
+    _, p = O.head_absorbed(rng.standard_normal(16), rng.standard_normal(8),
+                           rng.standard_normal((16, 32)), rng.standard_normal((16, 32)), c, kr, 0.2)
+    assert abs(p.sum() - 1) < 1e-13 and np.all(p >= 0)
+
+
+def test_append_rows_formats():
+    rng = np.random.default_rng(10)
+    c_raw, k_raw = rng.standard_normal((5, 256)), rng.standard_normal((5, 64))
+    pos = np.array([0, 1, 2, 100, 131071])
+    c, kr = O.rmsnorm(c_raw, 1e-6), O.rope(k_raw, pos, 1e4)
+    c32, k32, _ = O.append_rows(c_raw, k_raw, pos, cache_dtype="fp32", eps=1e-6, theta=1e4)
+    np.testing.assert_array_equal(c32, c.astype(np.float32))
+    np.testing.assert_array_equal(k32, kr.astype(np.float32))
+    cb, kb, _ = O.append_rows(c_raw, k_raw, pos, cache_dtype="bf16", eps=1e-6, theta=1e4)
+    np.testing.assert_array_equal(cb, O.round_to_bf16(c))
+    assert np.max(np.abs(cb - c) / np.abs(c)) <= 2.0**-8
+    c8, k8, extra = O.append_rows(c_raw, k_raw, pos, cache_dtype="fp8_e4m3_b128", eps=1e-6, theta=1e4)
+    np.testing.assert_array_equal(k8, kb)
+    np.testing.assert_array_equal(c8, extra["codes"] * np.repeat(extra["scales"].astype(np.float64), 128, axis=1))
+
+
+def test_page_slot_by_hand():
+    bt = np.array([[5, 2, 9], [0, 7, 1]], dtype=np.int32)
+    assert O.page_slot(bt, 0, 0, 64) == 5 * 64
+    assert O.page_slot(bt, 0, 63, 64) == 5 * 64 + 63
+    assert O.page_slot(bt, 0, 64, 64) == 2 * 64
+    assert O.page_slot(bt, 1, 130, 64) == 1 * 64 + 2
+
+
+# --------------------------------------------------------------- the pages' numbers
+
+def test_table1_mla_equals_gqa_with_2_25_groups():
+    f = json.load(open(os.path.join(GOLDEN, "pages_facts.json")))
+    m, t = f["v2_mla"], f["table1"]
+    assert m["d_c"] == t["d_c_over_d_h"] * m["d_h"] and m["d_h_R"] == t["d_h_R_over_d_h"] * m["d_h"]
+    mla = O.kv_elements_per_token("MLA", n_h=m["n_h"], d_h=m["d_h"], l=1, d_c=m["d_c"], d_r=m["d_h_R"])
+    gqa1 = O.kv_elements_per_token("GQA", n_h=m["n_h"], d_h=m["d_h"], l=1, n_g=1)
+    assert mla / gqa1 == t["gqa_equivalent_groups"]
+    assert O.kv_elements_per_token("MHA", n_h=128, d_h=128, l=60) / (mla * 60) == pytest.approx(2 * 128 / 4.5)
+
+
+def test_kv_cache_reduction_93_3_percent():
+    """93.3% follows from 60 layers x 576 elements x 6 bit against 95 layers x 8 groups x
+    2 x 128 x 16 bit (the 67B head dim 128 and bf16 cache are assumptions)."""
+    f = json.load(open(os.path.join(GOLDEN, "pages_facts.json")))
+    m, s, g = f["v2_mla"], f["serving"], f["llm_67b"]
+    v2 = O.kv_elements_per_token("MLA", n_h=m["n_h"], d_h=m["d_h"], l=m["layers"], d_c=m["d_c"],
+                                 d_r=m["d_h_R"]) * s["kv_bits_per_element_v2"]
+    ds67 = O.kv_elements_per_token("GQA", n_h=g["heads"], d_h=128, l=g["layers"], n_g=g["kv_groups"]) * 16
+    assert round(100 * (1 - v2 / ds67), 1) == s["kv_cache_reduction_vs_67b_percent"]
+
+
+def test_yarn_entropy_factor():
+    f = json.load(open(os.path.join(GOLDEN, "pages_facts.json")))
+    y = f["yarn"]
+    assert O.yarn_mscale_sqrt_t(y["s"]) == pytest.approx(y["sqrt_t_coeff"] * math.log(40) + 1)
+    assert O.yarn_mscale_sqrt_t(1.0) == 1.0
