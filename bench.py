@@ -1,0 +1,409 @@
+"""Benchmark of one MLA decode step on B300: append + decode over a paged latent cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole hot path over one batch: mla_append of the
+newest token of every sequence (latent RMSNorm, decoupled RoPE, paged row
+write) followed by mla_decode (W_UK absorption, attention over every cached
+token of every sequence, split combine and W_UV). The default workload is
+DeepSeek-V2-shaped decode (128 heads, 512 + 64 latent row, bf16, batch 16,
+4096 cached tokens per sequence, 64-token pages shuffled in the pool).
+
+Metric: cached tokens attended per second = sum_b L_b / step time. The cache
+and weights are resident in HBM; L2 is flushed (a 512 MiB memset) between
+timed steps, outside the timed events. Under torchrun every rank runs its own
+replica (weak scaling, no collective on the data path); rank 0 prints one
+JSON line.
+
+--impl reference times the fp64 CPU oracle (the slow, plain statement of the
+method) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_synth as S  # noqa: E402
+
+METRIC = "MLA decode cached-tokens attended/s on 1 B300; % of HBM/tensor roofline"
+UNIT = "tokens/s"
+FLOP_PER_HEAD_TOKEN = 2 * (576 + 512)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv2_b16", choices=sorted(S.SHAPES))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget per measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int):
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in self.rows for k in range(4) if r[3 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------- the GPU arm
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "head_latent_attention_22_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """dram bytes per launch of `kernel` from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path)).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_digest") != source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def peaks():
+    try:
+        p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def run_gpu(args, rank, world, local):
+    import head_latent_attention_22_b300 as M
+    from head_latent_attention_22_b300 import build as B
+    B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    init_dist(world)
+    shape = S.SHAPES[args.workload]
+    inp = S.make_inputs(shape)
+    cfg = M.MLAConfig.from_shape(shape)
+    B_, H = shape.batch, shape.n_heads
+    tokens = int(inp.lengths.sum())
+    max_len = int(inp.lengths.max())
+
+    # resident state: weights, page table, pool filled with every token
+    pool = M.new_pool(cfg, inp.num_pages, dev)
+    bt = torch.from_numpy(inp.block_table).to(dev)
+    seq_lens = torch.from_numpy(inp.lengths.astype(np.int32)).to(dev)
+    w_uk, w_uv = inp.w_uk.to(dev), inp.w_uv.to(dev)
+    pos_all = torch.from_numpy(inp.positions())
+    seq_all = torch.from_numpy(inp.seq_index())
+    chunk = 1 << 20
+    for s in range(0, tokens, chunk):
+        e = min(tokens, s + chunk)
+        M.append(cfg, inp.c_kv_raw[s:e].to(dev), inp.k_rope_raw[s:e].to(dev), pos_all[s:e].to(dev), pool, bt,
+                 seq_idx=seq_all[s:e].to(dev))
+    torch.cuda.synchronize()
+    del pos_all, seq_all
+
+    new_pos = torch.from_numpy((inp.lengths - 1).astype(np.int32)).to(dev)
+    new_seq = torch.arange(B_, dtype=torch.int32, device=dev)
+    out = torch.empty((B_, H, shape.d_head), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(256, M.workspace_size(cfg, B_, max_len)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    n_steps = args.warmup + args.steps
+    steps = [S.draw_step(inp, k) for k in range(min(n_steps, 8))]
+    dsteps = [tuple(t.to(dev) for t in (st.q_nope, st.q_rope, st.c_new, st.k_new)) for st in steps]
+    stream = torch.cuda.current_stream()
+
+    def step(k):
+        qn, qr, cn, kn = dsteps[k % len(dsteps)]
+        M.append(cfg, cn, kn, new_pos, pool, bt, seq_idx=new_seq)
+        M.decode(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+
+    launches_per_step = 1 + len(M.decode_stage_names(cfg))
+    for k in range(args.warmup):
+        step(k)
+        flush.zero_()
+    torch.cuda.synchronize()
+    M.check_device_errors()
+
+    # timed region: K steps, each bracketed by its own events; L2 flushed between steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            step(args.warmup + k)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    M.check_device_errors()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * tokens * args.steps / (total_ms / 1e3)
+
+    # per-kernel durations (separate pass, same steps, events between the kernels)
+    names = M.decode_stage_names(cfg)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.zero_()
+        M.set_stage_events(kev[k])
+        step(args.warmup + k)
+    M.set_stage_events(None)
+    torch.cuda.synchronize()
+    per_kernel = {n: statistics.mean(kev[k][i].elapsed_time(kev[k][i + 1]) for k in range(args.steps))
+                  for i, n in enumerate(names)}
+    dom = max(per_kernel, key=per_kernel.get)
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    row = M.cache_row_bytes(cfg)
+    attend_bytes = tokens * row + B_ * H * (shape.d_c + shape.d_rope) * 2
+    attend_flop = tokens * H * FLOP_PER_HEAD_TOKEN
+    weight_bytes = 2 * H * shape.d_head * shape.d_c * (2 if shape.io_dtype == "bf16" else 4)
+    if dom.startswith("attend"):
+        alg_bytes, alg_flop = attend_bytes, attend_flop
+    else:
+        alg_bytes, alg_flop = weight_bytes / 2, 2 * B_ * H * shape.d_head * shape.d_c
+    t = per_kernel[dom] / 1e3
+    ach_gbs = alg_bytes / t / 1e9
+    roofline = {"bound": "hbm", "achieved": round(ach_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach_gbs / hbm, 4), "traffic": committed_traffic(dom), "kernel": dom,
+                "kernel_ms": round(per_kernel[dom], 5), "algorithmic_bytes": alg_bytes,
+                "tensor_tflops": round(alg_flop / t / 1e12, 1), "tensor_peak": tf_burst,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind,
+                "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()}}
+    # whole-step roofline: the slower of all bytes over HBM and all FLOPs over the tensor peak
+    step_bytes = attend_bytes + weight_bytes + B_ * row
+    step_flop = attend_flop + 4 * B_ * H * shape.d_head * shape.d_c
+    t_roof = max(step_bytes / (hbm * 1e9), step_flop / (tf_burst * 1e12))
+    roofline["step_frac"] = round(t_roof / (ms_per_step / 1e3), 4)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    host = [tuple(t.pin_memory() for t in (st.q_nope, st.q_rope, st.c_new, st.k_new)) for st in steps]
+    dbuf = [torch.empty_like(t, device=dev) for t in host[0]]
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_s = 0.0
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for d, hsrc in zip(dbuf, host[k % len(host)]):
+            d.copy_(hsrc, non_blocking=True)
+        M.append(cfg, dbuf[2], dbuf[3], new_pos, pool, bt, seq_idx=new_seq)
+        M.decode(cfg, dbuf[0], dbuf[1], w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        if k >= args.warmup:
+            e2e_s += time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world, dev)
+    e2e = {"value": world * tokens * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_s / args.steps, 4)}
+
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": shape.io_dtype if shape.cache_dtype != "fp8_e4m3_b128"
+           else "bf16+fp8cache", "data": "synthetic (seeded; random-init weights)",
+           "config": {"workload": shape.name, "batch": B_, "seq_len": max_len, "cached_tokens": tokens,
+                      "n_heads": H, "d_c": shape.d_c, "d_rope": shape.d_rope, "d_head": shape.d_head,
+                      "page_size": shape.page_size, "cache_dtype": shape.cache_dtype,
+                      "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB memset)",
+                      "decode_path": "tcgen05" if M.decode_path(cfg) else "cuda-core"},
+           "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+           "clocks": clocks.summary()}
+    return res, inp
+
+
+# ----------------------------------------------------------------------------- the oracle arm
+
+def oracle_sample(inp, seconds: float, step: int = 0):
+    """Time the fp64 oracle on a bounded sample of one step: the append of every
+    sequence's newest token, then (sequence, head) decodes until the budget is used."""
+    from oracle import mla_oracle as O
+    s = inp.shape
+    st = S.draw_step(inp, step)
+    rng = np.random.default_rng(step)
+    w_uk = inp.w_uk.double().numpy()
+    w_uv = inp.w_uv.double().numpy()
+    qn, qr = st.q_nope.double().numpy(), st.q_rope.double().numpy()
+    # cache content of the sequences the sample touches (not timed: it is resident state)
+    order = [(int(b), int(i)) for b, i in zip(rng.integers(0, s.batch, 1 << 16), rng.integers(0, s.n_heads, 1 << 16))]
+    seqs = sorted({b for b, _ in order[:64]})
+    cache = {}
+    for b in seqs:
+        o0, o1 = int(inp.token_offsets[b]), int(inp.token_offsets[b + 1]) - 1
+        c, kr, _ = O.append_rows(inp.c_kv_raw[o0:o1].double().numpy(), inp.k_rope_raw[o0:o1].double().numpy(),
+                                 np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta)
+        cache[b] = (c, kr)
+    t0 = time.perf_counter()
+    c_new, k_new, _ = O.append_rows(st.c_new.double().numpy(), st.k_new.double().numpy(), inp.lengths - 1,
+                                    cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta)
+    done, tok = 0, 0
+    for b, i in order:
+        if b not in cache:
+            continue
+        c = np.concatenate([cache[b][0], c_new[b:b + 1]])
+        kr = np.concatenate([cache[b][1], k_new[b:b + 1]])
+        O.head_absorbed(qn[b, i], qr[b, i], w_uk[i], w_uv[i], c, kr, s.scale)
+        done += 1
+        tok += len(c)
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    # a token attended = one cached token for all heads of its sequence
+    return tok / s.n_heads / dt, done, dt
+
+
+def blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max([x.get("num_threads", 1) for x in info] or [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, seconds):
+    v, done, dt = oracle_sample(inp, seconds)
+    return {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{done} (sequence, head) decodes of {inp.shape.name} in the fp64 absorbed form "
+                      f"({dt:.1f} s), plus the append of the step's new tokens; tokens/s = cached tokens "
+                      f"visited / n_heads / time"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    shape = S.SHAPES[args.workload]
+    inp = S.make_inputs(shape)
+    for k in range(args.warmup):
+        oracle_sample(inp, min(1.0, args.cpu_seconds / 10), k)
+    vals, secs = [], 0.0
+    per_step = max(0.5, args.cpu_seconds / max(1, args.steps))
+    for k in range(args.steps):
+        v, done, dt = oracle_sample(inp, per_step, args.warmup + k)
+        vals.append(v)
+        secs += dt
+    value = float(np.mean(vals))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": shape.name, "batch": shape.batch, "seq_len": int(inp.lengths.max()),
+                       "cached_tokens": int(inp.lengths.sum()), "n_heads": shape.n_heads,
+                       "cache_dtype": shape.cache_dtype, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"each step: {per_step:.1f} s of (sequence, head) fp64 absorbed-form "
+                                       f"decodes of {shape.name}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res, inp = run_gpu(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

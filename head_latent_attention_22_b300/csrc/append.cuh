@@ -1,0 +1,211 @@
+// mla_append kernels: latent RMSNorm (DeepSeek-V2 report, section 3.1.2),
+// decoupled RoPE on the shared key (section 2.1.3) and the paged row write.
+// One warp per token. The vectorised kernel covers the DeepSeek-V2 row
+// (d_c = 512, d_rope = 64, bf16 inputs) with 16-byte loads and stores; the
+// scalar kernel covers every other shape.
+#pragma once
+
+#include "common.cuh"
+
+namespace mla {
+
+struct AppendArgs {
+  const void* c_raw;
+  const void* k_raw;
+  const int32_t* positions;
+  const int32_t* seq_idx;
+  const float* gamma;
+  uint8_t* pool;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int batch, max_pages, n_tokens, d_c, d_rope, page_size, cache_dtype, rope_interleaved;
+  float eps;
+  double log_theta;
+  int64_t row_bytes;
+};
+
+// Pool row of token t, or -1 (and the bounds bit) when any index is outside its array.
+__device__ __forceinline__ int64_t append_slot(const AppendArgs& a, int t, int* pos_out) {
+  const int pos = a.positions[t];
+  const int s = a.seq_idx ? a.seq_idx[t] : t;
+  if (s < 0 || s >= a.batch || pos < 0) return -1;
+  const int pg = pos / a.page_size;
+  if (pg >= a.max_pages) return -1;
+  const int64_t page = a.block_table ? static_cast<int64_t>(a.block_table[static_cast<int64_t>(s) * a.max_pages + pg])
+                                     : static_cast<int64_t>(s) * a.max_pages + pg;
+  if (page < 0 || page >= a.num_pages) return -1;
+  *pos_out = pos;
+  return page * a.page_size + pos % a.page_size;
+}
+
+// Rotation of pair m at position pos: angle pos * theta^(-2m/d) in fp64.
+__device__ __forceinline__ void rope_pair(double a, double b, int m, int d_rope, int pos,
+                                          double log_theta, double* ra, double* rb) {
+  const double inv_freq = exp(-(2.0 * m / d_rope) * log_theta);
+  double sn, cs;
+  sincos(static_cast<double>(pos) * inv_freq, &sn, &cs);
+  *ra = a * cs - b * sn;
+  *rb = a * sn + b * cs;
+}
+
+__device__ __forceinline__ uint16_t f64_to_bf16_bits(double d) {
+  __nv_bfloat16 h = __double2bfloat16(d);  // one rounding, to nearest even
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------- d_c = 512, d_rope = 64, bf16 in
+// Lane l owns latent elements [16 l, 16 l + 16) and rope pair l.
+template <int CACHE>  // MLA_DTYPE_BF16 or MLA_DTYPE_FP8_E4M3_B128
+__global__ void __launch_bounds__(256) append_dsv2_kernel(AppendArgs a) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= a.n_tokens) return;
+  int pos = 0;
+  const int64_t slot = append_slot(a, t, &pos);
+  if (slot < 0) {
+    if (lane == 0) flag_error(ERR_BIT_BOUNDS);
+    return;
+  }
+  uint8_t* row = a.pool + slot * a.row_bytes;
+
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.c_raw) +
+                                                    static_cast<int64_t>(t) * 512 + 16 * lane);
+  uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = bf16_to_f32(static_cast<uint16_t>(w[i] & 0xffffu));
+    x[2 * i + 1] = bf16_to_f32(static_cast<uint16_t>(w[i] >> 16));
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / 512.0f + a.eps);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float g = a.gamma ? a.gamma[16 * lane + i] : 1.0f;
+    x[i] = x[i] * inv * g;
+  }
+
+  int rope_off;
+  if constexpr (CACHE == MLA_DTYPE_BF16) {
+    uint4 o0, o1;
+    o0.x = pack_bf16x2(x[0], x[1]);   o0.y = pack_bf16x2(x[2], x[3]);
+    o0.z = pack_bf16x2(x[4], x[5]);   o0.w = pack_bf16x2(x[6], x[7]);
+    o1.x = pack_bf16x2(x[8], x[9]);   o1.y = pack_bf16x2(x[10], x[11]);
+    o1.z = pack_bf16x2(x[12], x[13]); o1.w = pack_bf16x2(x[14], x[15]);
+    uint4* dst = reinterpret_cast<uint4*>(row + 32 * lane);
+    dst[0] = o0;
+    dst[1] = o1;
+    rope_off = 1024;
+  } else {
+    // block of 128 values = lanes 8k .. 8k+7
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[4 * i], s), __fdiv_rn(x[4 * i + 1], s));
+      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[4 * i + 2], s), __fdiv_rn(x[4 * i + 3], s));
+      q[i] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
+    if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + 4 * (lane >> 3)) = s;
+    rope_off = 528;
+  }
+
+  const uint16_t* kr = static_cast<const uint16_t*>(a.k_raw) + static_cast<int64_t>(t) * 64;
+  uint16_t* kdst = reinterpret_cast<uint16_t*>(row + rope_off);
+  const int i0 = a.rope_interleaved ? 2 * lane : lane;
+  const int i1 = a.rope_interleaved ? 2 * lane + 1 : lane + 32;
+  double ra, rb;
+  rope_pair(bf16_to_f32(kr[i0]), bf16_to_f32(kr[i1]), lane, 64, pos, a.log_theta, &ra, &rb);
+  if (a.rope_interleaved) {
+    *reinterpret_cast<uint32_t*>(kdst + i0) =
+        static_cast<uint32_t>(f64_to_bf16_bits(ra)) | (static_cast<uint32_t>(f64_to_bf16_bits(rb)) << 16);
+  } else {
+    kdst[i0] = f64_to_bf16_bits(ra);
+    kdst[i1] = f64_to_bf16_bits(rb);
+  }
+}
+
+// ---------------------------------------------------------------- any shape (scalar)
+template <typename Tin>
+__global__ void __launch_bounds__(256) append_generic_kernel(AppendArgs a) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= a.n_tokens) return;
+  int pos = 0;
+  const int64_t slot = append_slot(a, t, &pos);
+  if (slot < 0) {
+    if (lane == 0) flag_error(ERR_BIT_BOUNDS);
+    return;
+  }
+  uint8_t* row = a.pool + slot * a.row_bytes;
+  const Tin* c = static_cast<const Tin*>(a.c_raw) + static_cast<int64_t>(t) * a.d_c;
+  const Tin* k = static_cast<const Tin*>(a.k_raw) + static_cast<int64_t>(t) * a.d_rope;
+
+  float ss = 0.f;
+  for (int i = lane; i < a.d_c; i += 32) {
+    const float x = load_as_f32(c, i);
+    ss = fmaf(x, x, ss);
+  }
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(a.d_c) + a.eps);
+  auto cval = [&](int i) { return load_as_f32(c, i) * inv * (a.gamma ? a.gamma[i] : 1.0f); };
+
+  int64_t rope_off = 0;
+  if (a.cache_dtype == MLA_DTYPE_FP32) {
+    float* dst = reinterpret_cast<float*>(row);
+    for (int i = lane; i < a.d_c; i += 32) dst[i] = cval(i);
+    rope_off = 4LL * a.d_c;
+  } else if (a.cache_dtype == MLA_DTYPE_BF16) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(row);
+    for (int i = lane; i < a.d_c; i += 32) dst[i] = f32_to_bf16_bits(cval(i));
+    rope_off = 2LL * a.d_c;
+  } else {  // FP8_E4M3_B128
+    float* scales = reinterpret_cast<float*>(row + a.d_c);
+    for (int blk = 0; blk < a.d_c / 128; ++blk) {
+      float amax = 0.f;
+      for (int i = blk * 128 + lane; i < blk * 128 + 128; i += 32) amax = fmaxf(amax, fabsf(cval(i)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float s = amax == 0.f ? 1.0f : __fdiv_rn(amax, 448.0f);
+      for (int i = blk * 128 + lane; i < blk * 128 + 128; i += 32)
+        row[i] = static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(cval(i), s), 0.f) & 0xffu);
+      if (lane == 0) scales[blk] = s;
+    }
+    rope_off = a.d_c + 4LL * (a.d_c / 128);
+  }
+
+  const int half = a.d_rope / 2;
+  for (int m = lane; m < half; m += 32) {
+    const int i0 = a.rope_interleaved ? 2 * m : m;
+    const int i1 = a.rope_interleaved ? 2 * m + 1 : m + half;
+    double ra, rb;
+    rope_pair(load_as_f32(k, i0), load_as_f32(k, i1), m, a.d_rope, pos, a.log_theta, &ra, &rb);
+    if (a.cache_dtype == MLA_DTYPE_FP32) {
+      float* dst = reinterpret_cast<float*>(row + rope_off);
+      dst[i0] = static_cast<float>(ra);
+      dst[i1] = static_cast<float>(rb);
+    } else {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(row + rope_off);
+      dst[i0] = f64_to_bf16_bits(ra);
+      dst[i1] = f64_to_bf16_bits(rb);
+    }
+  }
+}
+
+}  // namespace mla

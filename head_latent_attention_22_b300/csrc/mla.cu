@@ -1,0 +1,270 @@
+// Host side of the MLA C ABI (include/mla.h): argument checks, planning of
+// the split over sequence blocks, workspace layout and kernel launches. The
+// whole library is this one translation unit.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "append.cuh"
+#include "common.cuh"
+#include "decode_simt.cuh"
+
+namespace mla {
+namespace {
+
+thread_local std::string g_last_error;
+
+// Optional per-kernel timing events (see mla_set_stage_events).
+struct StageEvents {
+  cudaEvent_t ev[8];
+  int n = 0;
+};
+thread_local StageEvents g_stage;
+
+inline void stage_mark(int k, cudaStream_t st) {
+  if (k < g_stage.n) cudaEventRecord(g_stage.ev[k], st);
+}
+
+mla_status fail(mla_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mla_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status check_config(const mla_config* c) {
+  if (!c) return fail(MLA_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->n_heads < 1 || c->d_c < 1 || c->d_rope < 2 || (c->d_rope & 1) || c->d_head < 1 || c->page_size < 1)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: n_heads=%d d_c=%d d_rope=%d d_head=%d page_size=%d",
+                c->n_heads, c->d_c, c->d_rope, c->d_head, c->page_size);
+  if (c->io_dtype != MLA_DTYPE_BF16 && c->io_dtype != MLA_DTYPE_FP32)
+    return fail(MLA_ERR_INVALID_ARG, "io_dtype must be BF16 or FP32");
+  if (c->cache_dtype != MLA_DTYPE_BF16 && c->cache_dtype != MLA_DTYPE_FP32 &&
+      c->cache_dtype != MLA_DTYPE_FP8_E4M3_B128)
+    return fail(MLA_ERR_INVALID_ARG, "unknown cache_dtype %d", c->cache_dtype);
+  if (c->cache_dtype == MLA_DTYPE_FP8_E4M3_B128 && (c->d_c % 128) != 0)
+    return fail(MLA_ERR_INVALID_ARG, "FP8 cache needs d_c %% 128 == 0 (d_c=%d)", c->d_c);
+  if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f) || !std::isfinite(c->scale))
+    return fail(MLA_ERR_INVALID_ARG, "bad eps/rope_theta/scale");
+  return MLA_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ SIMT decode plan
+struct SimtPlan {
+  int n_splits, split_tokens;
+  size_t off_qlat, off_o, off_m, off_l, bytes;
+};
+
+SimtPlan simt_plan(const mla_config* c, int batch, int max_seq_len) {
+  SimtPlan p{};
+  const int L = max_seq_len < 1 ? 1 : max_seq_len;
+  int splits = (L + 511) / 512;
+  if (splits > 64) splits = 64;
+  if (splits < 1) splits = 1;
+  int per = (L + splits - 1) / splits;
+  per = (per + kSimtTileTokens - 1) / kSimtTileTokens * kSimtTileTokens;
+  splits = (L + per - 1) / per;
+  p.n_splits = splits;
+  p.split_tokens = per;
+  const size_t BH = static_cast<size_t>(batch) * c->n_heads;
+  size_t off = 0;
+  p.off_qlat = off;
+  off = align_up(off + BH * (c->d_c + c->d_rope) * 4, 256);
+  p.off_o = off;
+  off = align_up(off + BH * splits * c->d_c * 4, 256);
+  p.off_m = off;
+  off = align_up(off + BH * splits * 4, 256);
+  p.off_l = off;
+  off = align_up(off + BH * splits * 4, 256);
+  p.bytes = off;
+  return p;
+}
+
+mla_status decode_simt(const mla_config* c, const void* q_nope, const void* q_rope, const void* w_uk,
+                       const void* w_uv, const void* pool, int64_t num_pages, const int32_t* block_table,
+                       const int32_t* seq_lens, int batch, int max_pages, int max_seq_len, float* out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  if (c->d_c > kSimtMaxDc) return fail(MLA_ERR_UNSUPPORTED, "CUDA-core decode supports d_c <= %d", kSimtMaxDc);
+  const SimtPlan p = simt_plan(c, batch, max_seq_len);
+  if (workspace_bytes < p.bytes)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, p.bytes);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SimtArgs a{};
+  a.q_nope = q_nope; a.q_rope = q_rope; a.w_uk = w_uk; a.w_uv = w_uv;
+  a.pool = static_cast<const uint8_t*>(pool);
+  a.num_pages = num_pages; a.block_table = block_table; a.seq_lens = seq_lens;
+  a.batch = batch; a.max_pages = max_pages; a.n_heads = c->n_heads; a.d_c = c->d_c;
+  a.d_rope = c->d_rope; a.d_head = c->d_head; a.page_size = c->page_size;
+  a.cache_dtype = c->cache_dtype;
+  a.row_bytes = static_cast<int64_t>(row_bytes_of(c->cache_dtype, c->d_c, c->d_rope));
+  a.scale_log2 = c->scale * 1.4426950408889634f;
+  a.out = out;
+  a.q_lat = reinterpret_cast<float*>(ws + p.off_qlat);
+  a.part_o = reinterpret_cast<float*>(ws + p.off_o);
+  a.part_m = reinterpret_cast<float*>(ws + p.off_m);
+  a.part_l = reinterpret_cast<float*>(ws + p.off_l);
+  a.n_splits = p.n_splits;
+  a.split_tokens = p.split_tokens;
+  a.max_seq_len = max_seq_len;
+
+  const int D = c->d_c + c->d_rope;
+  const size_t smem_att = static_cast<size_t>(kSimtHeadsPerCta + kSimtTileTokens) * D * 4;
+  if (smem_att > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(attend_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_att));
+    if (e != cudaSuccess) return cuda_fail(e, "attend_simt smem attribute");
+  }
+  const dim3 g_abs(c->n_heads, batch);
+  stage_mark(0, st);
+  if (c->io_dtype == MLA_DTYPE_BF16)
+    absorb_simt_kernel<uint16_t><<<g_abs, 128, c->d_head * 4, st>>>(a);
+  else
+    absorb_simt_kernel<float><<<g_abs, 128, c->d_head * 4, st>>>(a);
+  stage_mark(1, st);
+  const dim3 g_att(p.n_splits, (c->n_heads + kSimtHeadsPerCta - 1) / kSimtHeadsPerCta, batch);
+  attend_simt_kernel<<<g_att, 32 * kSimtHeadsPerCta, smem_att, st>>>(a);
+  stage_mark(2, st);
+  if (c->io_dtype == MLA_DTYPE_BF16)
+    combine_simt_kernel<uint16_t><<<g_abs, 256, c->d_c * 4, st>>>(a);
+  else
+    combine_simt_kernel<float><<<g_abs, 256, c->d_c * 4, st>>>(a);
+  stage_mark(3, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode (CUDA-core) launch");
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+size_t mla_cache_row_bytes(const mla_config* cfg) {
+  if (check_config(cfg) != MLA_OK) return 0;
+  return row_bytes_of(cfg->cache_dtype, cfg->d_c, cfg->d_rope);
+}
+
+mla_status mla_append(const mla_config* cfg, const void* c_kv_raw, const void* k_rope_raw,
+                      const int32_t* positions, const int32_t* seq_idx, const float* gamma, void* pool,
+                      int64_t num_pages, const int32_t* block_table, int32_t batch, int32_t max_pages,
+                      int32_t n_tokens, void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (n_tokens < 0 || batch < 1 || max_pages < 1 || num_pages < 1)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: n_tokens=%d batch=%d max_pages=%d num_pages=%lld", n_tokens,
+                batch, max_pages, static_cast<long long>(num_pages));
+  if (n_tokens == 0) return MLA_OK;
+  if (!c_kv_raw || !k_rope_raw || !positions || !pool)
+    return fail(MLA_ERR_INVALID_ARG, "c_kv_raw, k_rope_raw, positions and pool must be non-NULL");
+  if (!aligned16(c_kv_raw) || !aligned16(k_rope_raw) || !aligned16(pool))
+    return fail(MLA_ERR_INVALID_ARG, "c_kv_raw, k_rope_raw and pool must be 16-byte aligned");
+  AppendArgs a{};
+  a.c_raw = c_kv_raw; a.k_raw = k_rope_raw; a.positions = positions; a.seq_idx = seq_idx; a.gamma = gamma;
+  a.pool = static_cast<uint8_t*>(pool); a.num_pages = num_pages; a.block_table = block_table;
+  a.batch = batch; a.max_pages = max_pages; a.n_tokens = n_tokens; a.d_c = cfg->d_c; a.d_rope = cfg->d_rope;
+  a.page_size = cfg->page_size; a.cache_dtype = cfg->cache_dtype; a.rope_interleaved = cfg->rope_interleaved;
+  a.eps = cfg->eps; a.log_theta = std::log(static_cast<double>(cfg->rope_theta));
+  a.row_bytes = static_cast<int64_t>(row_bytes_of(cfg->cache_dtype, cfg->d_c, cfg->d_rope));
+  const cudaStream_t st = as_stream(stream);
+  const int threads = 256, warps = threads / 32;
+  const int blocks = (n_tokens + warps - 1) / warps;
+  const bool dsv2 = cfg->io_dtype == MLA_DTYPE_BF16 && cfg->d_c == 512 && cfg->d_rope == 64 &&
+                    (cfg->cache_dtype == MLA_DTYPE_BF16 || cfg->cache_dtype == MLA_DTYPE_FP8_E4M3_B128);
+  if (dsv2 && cfg->cache_dtype == MLA_DTYPE_BF16)
+    append_dsv2_kernel<MLA_DTYPE_BF16><<<blocks, threads, 0, st>>>(a);
+  else if (dsv2)
+    append_dsv2_kernel<MLA_DTYPE_FP8_E4M3_B128><<<blocks, threads, 0, st>>>(a);
+  else if (cfg->io_dtype == MLA_DTYPE_BF16)
+    append_generic_kernel<uint16_t><<<blocks, threads, 0, st>>>(a);
+  else
+    append_generic_kernel<float><<<blocks, threads, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return MLA_OK;
+}
+
+size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len) {
+  if (check_config(cfg) != MLA_OK || batch < 1) return 0;
+  return simt_plan(cfg, batch, max_seq_len).bytes;
+}
+
+int32_t mla_decode_path(const mla_config* cfg) {
+  (void)cfg;
+  return 0;
+}
+
+mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
+                      const void* w_uv, const void* pool, int64_t num_pages, const int32_t* block_table,
+                      const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t max_seq_len,
+                      float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (batch < 1 || max_pages < 1 || num_pages < 1 || max_seq_len < 0)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: batch=%d max_pages=%d num_pages=%lld max_seq_len=%d", batch,
+                max_pages, static_cast<long long>(num_pages), max_seq_len);
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * cfg->page_size)
+    return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (!q_nope || !q_rope || !w_uk || !w_uv || !pool || !seq_lens || !out || !workspace)
+    return fail(MLA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(pool) ||
+      !aligned16(out) || !aligned16(workspace))
+    return fail(MLA_ERR_INVALID_ARG, "q_nope, q_rope, w_uk, w_uv, pool, out and workspace must be 16-byte aligned");
+  return decode_simt(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
+                     max_seq_len, out, workspace, workspace_bytes, as_stream(stream));
+}
+
+mla_status mla_check_device_errors(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned int word = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&word, g_dev_error, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (word == 0) return MLA_OK;
+  e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero));
+  if (e != cudaSuccess) return cuda_fail(e, "clear device error word");
+  if (word & ERR_BIT_TIMEOUT) return fail(MLA_ERR_TIMEOUT, "a device-side wait ran out (word=0x%x)", word);
+  return fail(MLA_ERR_BOUNDS, "a device-side index was out of range (word=0x%x)", word);
+}
+
+const char* mla_decode_stage_names(const mla_config* cfg) {
+  (void)cfg;
+  return "absorb_simt,attend_simt,combine_simt";
+}
+
+mla_status mla_set_stage_events(void* const* events, int32_t n_events) {
+  if (n_events < 0 || n_events > 8) return fail(MLA_ERR_INVALID_ARG, "n_events must be in [0, 8]");
+  if (!events) n_events = 0;
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return fail(MLA_ERR_INVALID_ARG, "event %d is NULL", i);
+    g_stage.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_stage.n = n_events;
+  return MLA_OK;
+}
+
+const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

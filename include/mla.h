@@ -1,0 +1,182 @@
+/*
+ * mla.h - C ABI of the B300 (sm_103a) MLA decode library (libmla.so).
+ *
+ * Multi-head Latent Attention decode over a paged latent KV cache, as the
+ * DeepSeek-V2 report (translated page) states it in section 2.1:
+ *   - 2.1.2 low-rank joint KV compression: only a d_c-wide latent c_j is
+ *     cached per token; keys and values are its up-projections W_UK c_j and
+ *     W_UV c_j, and because W_UK can be absorbed into the query and W_UV
+ *     into the output, no per-head key or value is ever formed;
+ *   - 2.1.3 decoupled RoPE: a d_rope-wide key k^R_j = RoPE(k_raw_j), shared by
+ *     all heads, is cached beside c_j, so a row holds (d_c + d_rope) values;
+ *   - 3.1.2 an RMSNorm follows the compressed latent.
+ * Page tables (fixed-size pages of cache rows, a per-sequence list of page
+ * ids) are this library's storage layout; the report does not describe one.
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless
+ *     stated otherwise. The library allocates no device memory and keeps no
+ *     pointer after a call returns.
+ *   - Arrays are dense, row-major, innermost dimension contiguous; base
+ *     pointers of the pool, the raw inputs, the queries, the weights, `out`
+ *     and `workspace` must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream). The returned status covers host-side argument checks
+ *     and launch errors only. Errors found on the device (a page id outside
+ *     the pool, a position beyond the page table, a bounded wait that ran
+ *     out) skip the offending access and set a per-device error word, which
+ *     mla_check_device_errors() reads and clears.
+ *   - On any status other than MLA_OK, mla_last_error() returns a message
+ *     (thread-local; valid until the next call on the same thread).
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* a null/misaligned pointer, a bad size or config */
+  MLA_ERR_UNSUPPORTED = 2,  /* a config no kernel here implements */
+  MLA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MLA_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out */
+  MLA_ERR_BOUNDS = 5        /* a device-side index fell outside its array */
+} mla_status;
+
+typedef enum {
+  MLA_DTYPE_BF16 = 0,
+  MLA_DTYPE_FP32 = 1,
+  /* cache only: per row, d_c E4M3 codes, then d_c/128 fp32 scales (one per
+     128-value block: value = code * scale), then d_rope bf16 rope values */
+  MLA_DTYPE_FP8_E4M3_B128 = 2
+} mla_dtype;
+
+typedef struct {
+  int32_t n_heads;          /* n_h, query heads */
+  int32_t d_c;              /* latent width (KV compression dim) */
+  int32_t d_rope;           /* decoupled rope width d_h^R (even) */
+  int32_t d_head;           /* d_h, width of q_nope and of each head's output */
+  int32_t page_size;        /* tokens per cache page */
+  int32_t io_dtype;         /* mla_dtype of queries, weights, raw latents/keys: BF16 or FP32 */
+  int32_t cache_dtype;      /* mla_dtype of the pool rows */
+  float scale;              /* softmax scale applied to q.k (e.g. 1/sqrt(d_h + d_rope)) */
+  float eps;                /* RMSNorm epsilon */
+  float rope_theta;         /* RoPE base; pair m turns by pos * theta^(-2m/d_rope) */
+  int32_t rope_interleaved; /* 1: pairs (2m, 2m+1) (RoFormer); 0: pairs (m, m + d_rope/2) */
+} mla_config;
+
+/* Bytes of one cache row for `cfg` (0 if cfg is invalid):
+   BF16 (d_c + d_rope) * 2; FP32 (d_c + d_rope) * 4;
+   FP8_E4M3_B128 d_c + 4 * d_c / 128 + 2 * d_rope. */
+MLA_API size_t mla_cache_row_bytes(const mla_config* cfg);
+
+/*
+ * mla_append - write n_tokens new tokens into the paged latent cache.
+ *
+ * Computes, per token t (report sections 3.1.2 and 2.1.3):
+ *   c  = c_kv_raw[t] / sqrt(mean(c_kv_raw[t]^2) + eps) * gamma   (fp32 math)
+ *   kR = RoPE(k_rope_raw[t], positions[t])   (angle and rotation in fp64)
+ * and stores (c, kR), converted to the cache format, as the row
+ *   slot = block_table[s * max_pages + positions[t] / page_size] * page_size
+ *          + positions[t] % page_size,   s = seq_idx ? seq_idx[t] : t.
+ * Conversion is round-to-nearest-even (bf16) or, for FP8_E4M3_B128, per
+ * 128-value block scale = amax / 448 (1 if amax == 0) and code =
+ * E4M3_satfinite_RNE(c / scale) with an IEEE fp32 division.
+ *
+ *   c_kv_raw   [n_tokens, d_c]    io_dtype
+ *   k_rope_raw [n_tokens, d_rope] io_dtype
+ *   positions  [n_tokens] int32   0-based position in its sequence
+ *   seq_idx    [n_tokens] int32 or NULL (token t belongs to sequence t)
+ *   gamma      [d_c] fp32 RMSNorm gain, or NULL (all ones)
+ *   pool       [num_pages, page_size, row_bytes] bytes, written
+ *   block_table[batch, max_pages] int32, or NULL: sequence s then owns pages
+ *              s*max_pages .. s*max_pages + max_pages-1 (contiguous layout)
+ * A token whose sequence, position or page id falls outside these arrays is
+ * not written and sets MLA_ERR_BOUNDS in the device error word. Two tokens
+ * given the same slot in one call race.
+ */
+MLA_API mla_status mla_append(const mla_config* cfg, const void* c_kv_raw, const void* k_rope_raw,
+                      const int32_t* positions, const int32_t* seq_idx, const float* gamma,
+                      void* pool, int64_t num_pages, const int32_t* block_table,
+                      int32_t batch, int32_t max_pages, int32_t n_tokens, void* stream);
+
+/*
+ * Bytes of scratch memory mla_decode needs for `batch` sequences whose
+ * lengths are at most max_seq_len, on the current device. The caller
+ * allocates it (any contents; 256-byte alignment).
+ */
+MLA_API size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len);
+
+/*
+ * mla_decode - one decode step of MLA over the paged latent cache.
+ *
+ * For each sequence b < batch and head i < n_heads (report section 2.1.2,
+ * absorbed form; section 2.1.3 decoupled RoPE):
+ *   q_lat   = W_UK[i]^T q_nope[b,i]                       (d_c)
+ *   s_j     = scale * (q_lat . c_j + q_rope[b,i] . kR_j),  j < seq_lens[b]
+ *   p       = softmax_j(s)
+ *   out[b,i]= W_UV[i] (sum_j p_j c_j)                     (d_head, fp32)
+ * where (c_j, kR_j) is cache row j of sequence b, found through block_table
+ * as in mla_append. seq_lens[b] == 0 gives zeros.
+ *
+ *   q_nope  [batch, n_heads, d_head] io_dtype
+ *   q_rope  [batch, n_heads, d_rope] io_dtype, already rotated
+ *   w_uk    [n_heads, d_head, d_c]   io_dtype  (head i = rows i*d_head.. of W_UK)
+ *   w_uv    [n_heads, d_head, d_c]   io_dtype
+ *   pool, num_pages, block_table, max_pages: as in mla_append (read only)
+ *   seq_lens[batch] int32 (device)
+ *   max_seq_len  host-side upper bound of seq_lens (plans the split over
+ *                sequence blocks; a larger device value sets MLA_ERR_BOUNDS
+ *                and is clamped)
+ *   out     [batch, n_heads, d_head] fp32, written
+ *   workspace, workspace_bytes: at least mla_decode_workspace_size() bytes
+ * Pages of a sequence are processed in independent splits whose partial
+ * results are merged by a log-sum-exp combine before W_UV is applied.
+ */
+MLA_API mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_rope,
+                      const void* w_uk, const void* w_uv, const void* pool, int64_t num_pages,
+                      const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                      int32_t max_pages, int32_t max_seq_len, float* out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
+ * Waits for `stream`, then returns and clears the current device's error
+ * word: MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (timeout wins if both).
+ */
+MLA_API mla_status mla_check_device_errors(void* stream);
+
+/* Which kernels mla_decode would use for cfg on the current device:
+   1 = tcgen05/TMA tensor-core path, 0 = CUDA-core (SIMT) path. */
+MLA_API int32_t mla_decode_path(const mla_config* cfg);
+
+/* Kernel names of one mla_decode call for cfg, in launch order, comma
+   separated (e.g. "absorb,attend,combine"); static storage. */
+MLA_API const char* mla_decode_stage_names(const mla_config* cfg);
+
+/*
+ * Timing hook. After this call, every mla_decode on the calling thread
+ * records events[0] on its stream before its first kernel and events[k]
+ * after its k-th kernel, for k < n_events (cudaEvent_t handles owned by the
+ * caller). n_events = 0 (or events = NULL) turns the hook off. At most 8.
+ */
+MLA_API mla_status mla_set_stage_events(void* const* events, int32_t n_events);
+
+/* Thread-local message describing the last non-OK status. */
+MLA_API const char* mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

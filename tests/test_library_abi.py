@@ -1,0 +1,98 @@
+"""The C-ABI library without a GPU: it loads, exports what include/mla.h
+declares, lays out the config struct as C does, and rejects bad arguments on
+the host before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import head_latent_attention_22_b300 as M
+from head_latent_attention_22_b300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ctypes.CDLL(M.library_path())
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        names |= set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"mla_append", "mla_decode", "mla_decode_workspace_size", "mla_check_device_errors",
+            "mla_cache_row_bytes", "mla_last_error", "mla_decode_path"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", M.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(mla_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        getattr(lib, n)
+
+
+def test_config_struct_layout_matches_c():
+    src = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "mla.h"
+int main(void) {
+  printf("%zu %zu %zu %zu\n", sizeof(mla_config), offsetof(mla_config, scale),
+         offsetof(mla_config, rope_theta), offsetof(mla_config, rope_interleaved));
+  return 0;
+}
+'''
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        open(c, "w").write(src)
+        exe = os.path.join(d, "t")
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
+    cc = M._CConfig
+    assert got == [ctypes.sizeof(cc), cc.scale.offset, cc.rope_theta.offset, cc.rope_interleaved.offset]
+
+
+def test_row_bytes():
+    assert M.cache_row_bytes(M.MLAConfig.dsv2()) == 1152
+    assert M.cache_row_bytes(M.MLAConfig.dsv2(M.FP8_E4M3_B128)) == 512 + 16 + 128
+    assert M.cache_row_bytes(M.MLAConfig(4, 32, 8, 16, 64, M.FP32, M.FP32)) == 160
+
+
+def test_host_rejects_bad_config_and_arguments(lib):
+    M._load()
+    cfg = M.MLAConfig.dsv2().c()
+    bad = M.MLAConfig(4, 32, 7, 16).c()        # odd rope width
+    assert M._load().mla_cache_row_bytes(ctypes.byref(bad)) == 0
+    assert M._load().mla_decode_workspace_size(ctypes.byref(bad), 4, 100) == 0
+    fp8_bad = M.MLAConfig(4, 96, 8, 16, 64, M.BF16, M.FP8_E4M3_B128).c()   # d_c not a multiple of 128
+    assert M._load().mla_cache_row_bytes(ctypes.byref(fp8_bad)) == 0
+    # NULL pointers and misaligned pointers are refused before any CUDA call
+    st = M._load().mla_append(ctypes.byref(cfg), None, None, None, None, None, None, 10, None, 4, 4, 4, None)
+    assert st == 1 and b"non-NULL" in M._load().mla_last_error()
+    st = M._load().mla_append(ctypes.byref(cfg), ctypes.c_void_p(8), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                              None, None, ctypes.c_void_p(16), 10, None, 4, 4, 4, None)
+    assert st == 1 and b"aligned" in M._load().mla_last_error()
+    st = M._load().mla_decode(ctypes.byref(cfg), None, None, None, None, None, 10, None, None, 4, 4, 100,
+                              None, None, 0, None)
+    assert st == 1
+    # a length bound beyond the page table's reach
+    st = M._load().mla_decode(ctypes.byref(cfg), *([ctypes.c_void_p(256)] * 5), 10, None, ctypes.c_void_p(256),
+                              4, 2, 129, ctypes.c_void_p(256), ctypes.c_void_p(256), 1 << 30, None)
+    assert st == 1 and b"max_seq_len" in M._load().mla_last_error()
+
+
+def test_workspace_size_grows_with_batch_and_length():
+    cfg = M.MLAConfig.dsv2()
+    a = M.workspace_size(cfg, 4, 4096)
+    assert a > 0 and M.workspace_size(cfg, 8, 4096) > a and M.workspace_size(cfg, 4, 131072) >= a
