@@ -22,7 +22,7 @@ import torch
 
 __all__ = ["MLAConfig", "MLAError", "BF16", "FP32", "FP8_E4M3_B128", "library_path", "cache_row_bytes",
            "new_pool", "append", "workspace_size", "decode", "check_device_errors", "decode_path",
-           "decode_stage_names", "set_stage_events"]
+           "decode_stage_names", "set_stage_events", "decode_static_scratch"]
 
 BF16, FP32, FP8_E4M3_B128 = 0, 1, 2
 _DTYPE_NAMES = {"bf16": BF16, "fp32": FP32, "fp8_e4m3_b128": FP8_E4M3_B128}
@@ -108,6 +108,7 @@ def _load():
         "mla_decode_path": (I32, [CFG]),
         "mla_last_error": (ctypes.c_char_p, []),
         "mla_decode_stage_names": (ctypes.c_char_p, [CFG]),
+        "mla_decode_static_scratch": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, P, P]),
         "mla_set_stage_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
     }
     for name, (res, args) in sig.items():
@@ -245,6 +246,34 @@ def set_stage_events(events) -> None:
             e.record()
     arr = (ctypes.c_void_p * max(1, len(events)))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(_load().mla_set_stage_events(arr, len(events)))
+
+
+def decode_static_scratch(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: torch.Tensor,
+                          w_uv: torch.Tensor, pool: torch.Tensor, block_table: Optional[torch.Tensor],
+                          seq_lens: torch.Tensor, max_seq_len: int, out: torch.Tensor,
+                          max_pages: Optional[int] = None, stream=None) -> torch.Tensor:
+    """mla_decode_static_scratch: the decode for callers that cannot allocate device memory.
+
+    Nothing is allocated, neither here nor in the library: the caller passes
+    `out`, and the library's fixed per-device scratch array replaces the
+    workspace. Calls on one device share that array and must not overlap.
+    """
+    dt = cfg.io_torch_dtype
+    for t, n, d in ((q_nope, "q_nope", dt), (q_rope, "q_rope", dt), (w_uk, "w_uk", dt), (w_uv, "w_uv", dt),
+                    (pool, "pool", torch.uint8), (seq_lens, "seq_lens", torch.int32), (out, "out", torch.float32)):
+        _need(t, n, d)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        max_pages = block_table.shape[1]
+    if max_pages is None:
+        raise ValueError("max_pages is needed without a block table")
+    if out.shape != (q_nope.shape[0], cfg.n_heads, cfg.d_head):
+        raise ValueError("out must be [batch, n_heads, d_head]")
+    _check(_load().mla_decode_static_scratch(ctypes.byref(cfg.c()), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk),
+                                             _ptr(w_uv), _ptr(pool), pool.shape[0], _ptr(block_table),
+                                             _ptr(seq_lens), q_nope.shape[0], max_pages, max_seq_len, _ptr(out),
+                                             _stream(stream)))
+    return out
 
 
 def check_device_errors(stream=None) -> None:

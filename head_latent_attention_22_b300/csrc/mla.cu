@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "append.cuh"
@@ -155,6 +156,32 @@ mla_status decode_simt(const mla_config* c, const void* q_nope, const void* q_ro
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------ fixed scratch
+// Scratch of mla_decode_static_scratch: one array per device, for callers
+// that cannot allocate. Host code must not use the symbol as an address; the
+// device address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_static_scratch[MLA_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_addr[kMaxDevices] = {};
+
+mla_status static_scratch_address(void** addr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device %d beyond %d devices", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_static_scratch_addr[dev] = p;
+  }
+  *addr = g_static_scratch_addr[dev];
+  return MLA_OK;
+}
+
 }  // namespace
 }  // namespace mla
 
@@ -234,6 +261,24 @@ mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_r
     return fail(MLA_ERR_INVALID_ARG, "q_nope, q_rope, w_uk, w_uv, pool, out and workspace must be 16-byte aligned");
   return decode_simt(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
                      max_seq_len, out, workspace, workspace_bytes, as_stream(stream));
+}
+
+mla_status mla_decode_static_scratch(const mla_config* cfg, const void* q_nope, const void* q_rope,
+                                     const void* w_uk, const void* w_uv, const void* pool, int64_t num_pages,
+                                     const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                                     int32_t max_pages, int32_t max_seq_len, float* out, void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (batch < 1 || max_seq_len < 0) return fail(MLA_ERR_INVALID_ARG, "bad sizes: batch=%d max_seq_len=%d", batch, max_seq_len);
+  const size_t need = mla_decode_workspace_size(cfg, batch, max_seq_len);
+  if (need > MLA_STATIC_SCRATCH_BYTES)
+    return fail(MLA_ERR_INVALID_ARG, "this decode needs %zu bytes of scratch; the fixed array holds %zu", need,
+                static_cast<size_t>(MLA_STATIC_SCRATCH_BYTES));
+  void* scratch = nullptr;
+  s = static_scratch_address(&scratch);
+  if (s != MLA_OK) return s;
+  return mla_decode(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
+                    max_seq_len, out, scratch, MLA_STATIC_SCRATCH_BYTES, stream);
 }
 
 mla_status mla_check_device_errors(void* stream) {

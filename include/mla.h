@@ -151,6 +151,37 @@ MLA_API mla_status mla_decode(const mla_config* cfg, const void* q_nope, const v
                       size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_static_scratch - mla_decode that allocates nothing and takes no
+ * workspace argument. The paper has no counterpart to this call; it exists
+ * for callers of this library that cannot allocate device memory at the
+ * point where they decode, e.g. a plugin running inside a host program that
+ * owns all device memory and offers it no allocator, or a serving loop whose
+ * memory plan is fixed up front and which must not call cudaMalloc (that
+ * call can synchronise the device and stall other streams).
+ *
+ * Arguments, results and errors are those of mla_decode, minus workspace.
+ * The scratch is one device array inside the library of
+ * MLA_STATIC_SCRATCH_BYTES (48 MiB); every GPU that loads the library holds
+ * it until the process exits. A request needing more scratch than that
+ * (mla_decode_workspace_size() > MLA_STATIC_SCRATCH_BYTES) is refused with
+ * MLA_ERR_INVALID_ARG before anything is launched; nothing is allocated.
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; make that first call
+ * before any stream capture. All calls on a device share the one array, so
+ * two calls whose kernels overlap on the GPU (different streams, or threads
+ * without ordering) race on it and both results are undefined; serialise
+ * them. The array keeps the last call's contents; the decode writes every
+ * scratch location before reading it, so nothing needs clearing between calls.
+ */
+#define MLA_STATIC_SCRATCH_BYTES ((size_t)48 << 20)
+MLA_API mla_status mla_decode_static_scratch(const mla_config* cfg, const void* q_nope, const void* q_rope,
+                                             const void* w_uk, const void* w_uv, const void* pool,
+                                             int64_t num_pages, const int32_t* block_table,
+                                             const int32_t* seq_lens, int32_t batch, int32_t max_pages,
+                                             int32_t max_seq_len, float* out, void* stream);
+
+/*
  * Waits for `stream`, then returns and clears the current device's error
  * word: MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (timeout wins if both).
  */
