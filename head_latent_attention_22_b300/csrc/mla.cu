@@ -10,6 +10,8 @@
 #include "append.cuh"
 #include "common.cuh"
 #include "decode_simt.cuh"
+#include "decode_tc.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -156,6 +158,178 @@ mla_status decode_simt(const mla_config* c, const void* q_nope, const void* q_ro
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------ tensor-core decode
+// The tcgen05 kernels cover the DeepSeek-V2 shape with bf16 queries, weights
+// and cache, and pages holding whole 64-token tiles.
+bool tc_supported(const mla_config* c) {
+  return c->n_heads == tcd::kH && c->d_c == tcd::kDc && c->d_rope == tcd::kDr && c->d_head == tcd::kDh &&
+         c->io_dtype == MLA_DTYPE_BF16 && c->cache_dtype == MLA_DTYPE_BF16 && c->page_size % tcd::kTile == 0;
+}
+
+// Clusters the workspace is sized for; a launch never uses more.
+constexpr int kMaxClusters = 128;
+
+struct TcPlan {
+  int nb, slots;
+  size_t off_qlat, off_lens, off_cum, off_ml, off_o, bytes;
+};
+
+TcPlan tc_plan(int batch) {
+  TcPlan p{};
+  p.nb = batch >= 128 ? 128 : (batch + 15) / 16 * 16;
+  p.slots = batch + kMaxClusters - 1;
+  size_t off = 0;
+  p.off_qlat = off;
+  off = align_up(off + static_cast<size_t>(batch) * tcd::kH * tcd::kRow * 2, 256);
+  p.off_lens = off;
+  off = align_up(off + static_cast<size_t>(batch) * 4, 256);
+  p.off_cum = off;
+  off = align_up(off + static_cast<size_t>(batch + 1) * 4, 256);
+  p.off_ml = off;
+  off = align_up(off + static_cast<size_t>(p.slots) * tcd::kH * 8, 256);
+  p.off_o = off;
+  off = align_up(off + static_cast<size_t>(p.slots) * tcd::kH * tcd::kDc * 4, 256);
+  p.bytes = off;
+  return p;
+}
+
+constexpr size_t kAttendSmem = 1024 + tcd::kStages * tcd::kStageBytes + tcd::kXbufBytes + sizeof(tcd::AttendSmem);
+constexpr size_t kCombineSmem = 1024 + tcd::kCombineSmem;
+size_t absorb_smem(int nb) { return 1024 + 8 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
+
+struct TcDeviceState {
+  bool ready = false;
+  int clusters = 0;
+};
+std::mutex g_tc_mu;
+TcDeviceState g_tc_state[64];
+
+// Per device, once: shared-memory limits of the three kernels and the number
+// of two-CTA clusters of the attend kernel that fit on the GPU at once.
+mla_status tc_device_setup(int* clusters) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device %d beyond 64 devices", dev);
+  std::lock_guard<std::mutex> lock(g_tc_mu);
+  TcDeviceState& st = g_tc_state[dev];
+  if (!st.ready) {
+    if ((e = cudaFuncSetAttribute(tcd::absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(absorb_smem(128)))) != cudaSuccess)
+      return cuda_fail(e, "absorb smem attribute");
+    if ((e = cudaFuncSetAttribute(tcd::attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kAttendSmem))) != cudaSuccess)
+      return cuda_fail(e, "attend smem attribute");
+    if ((e = cudaFuncSetAttribute(tcd::combine_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kCombineSmem))) != cudaSuccess)
+      return cuda_fail(e, "combine smem attribute");
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * kMaxClusters);
+    lc.blockDim = dim3(tcd::kAttendThreads);
+    lc.dynamicSmemBytes = kAttendSmem;
+    int n = 0;
+    if ((e = cudaOccupancyMaxActiveClusters(&n, tcd::attend_tc_kernel, &lc)) != cudaSuccess || n < 1)
+      return cuda_fail(e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "attend cluster occupancy");
+    const int half_sms = current_sm_count() / 2;
+    n = n < half_sms ? n : half_sms;
+    st.clusters = n < kMaxClusters ? n : kMaxClusters;
+    st.ready = true;
+  }
+  *clusters = st.clusters;
+  return MLA_OK;
+}
+
+mla_status launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = g_stage.n > 0 ? 0 : 1;   // per-kernel timing wants the kernels apart
+  cudaError_t e = cudaLaunchKernelExC(&lc, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core decode launch");
+  return MLA_OK;
+}
+
+mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope, const void* w_uk, const void* w_uv,
+                     const void* pool, int64_t num_pages, const int32_t* block_table, const int32_t* seq_lens,
+                     int batch, int max_pages, int max_seq_len, float* out, void* workspace, size_t workspace_bytes,
+                     cudaStream_t st) {
+  const TcPlan p = tc_plan(batch);
+  if (workspace_bytes < p.bytes)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, p.bytes);
+  const int64_t pool_rows = num_pages * static_cast<int64_t>(c->page_size);
+  if (pool_rows >= (static_cast<int64_t>(1) << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "pool of %lld rows exceeds the 2^31 rows a tile coordinate can address",
+                static_cast<long long>(pool_rows));
+  int ncl = 0;
+  mla_status s = tc_device_setup(&ncl);
+  if (s != MLA_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  tcd::Plan plan{reinterpret_cast<int32_t*>(ws + p.off_lens), reinterpret_cast<int32_t*>(ws + p.off_cum)};
+  uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
+
+  CUtensorMap m_pool, m_wuk, m_wuv, m_qn;
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_map_2d(&m_pool, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, tcd::kTile, SW) ||
+      !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
+      !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
+      !make_map_2d(&m_qn, q_nope, BF, tcd::kH * tcd::kDh, static_cast<uint64_t>(batch), tcd::kH * tcd::kDh * 2, 64,
+                   static_cast<uint32_t>(p.nb), SW))
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled refused a tensor description (or the driver entry point is missing)");
+
+  tcd::AbsorbArgs aa{};
+  aa.q_rope = static_cast<const uint16_t*>(q_rope);
+  aa.seq_lens = seq_lens;
+  aa.q_lat = q_lat;
+  aa.plan = plan;
+  aa.batch = batch;
+  aa.nb = p.nb;
+  aa.max_seq_len = max_seq_len;
+
+  tcd::AttendArgs ta{};
+  ta.q_lat = q_lat;
+  ta.block_table = block_table;
+  ta.plan = plan;
+  ta.part_o = reinterpret_cast<float*>(ws + p.off_o);
+  ta.part_ml = reinterpret_cast<float*>(ws + p.off_ml);
+  ta.num_pages = num_pages;
+  ta.batch = batch;
+  ta.max_pages = max_pages;
+  ta.page_size = c->page_size;
+  ta.scale_log2 = c->scale * 1.4426950408889634f;
+
+  tcd::CombineArgs ca{};
+  ca.plan = plan;
+  ca.part_o = ta.part_o;
+  ca.part_ml = ta.part_ml;
+  ca.out = out;
+  ca.batch = batch;
+  ca.ncl = ncl;
+
+  stage_mark(0, st);
+  tcd::absorb_tc_kernel<<<tcd::kH + 1, tcd::kAbsorbThreads, absorb_smem(p.nb), st>>>(m_wuk, m_qn, aa);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "absorb launch");
+  stage_mark(1, st);
+  void* attend_args[] = {&m_pool, &ta};
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_tc_kernel), dim3(2 * ncl), dim3(tcd::kAttendThreads),
+                 kAttendSmem, st, attend_args);
+  if (s != MLA_OK) return s;
+  stage_mark(2, st);
+  void* combine_args[] = {&m_wuv, &ca};
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::combine_tc_kernel), dim3(tcd::kH), dim3(tcd::kCombineThreads),
+                 kCombineSmem, st, combine_args);
+  if (s != MLA_OK) return s;
+  stage_mark(3, st);
+  return MLA_OK;
+}
+
 // ------------------------------------------------------------------ fixed scratch
 // Scratch of mla_decode_static_scratch: one array per device, for callers
 // that cannot allocate. Host code must not use the symbol as an address; the
@@ -235,12 +409,13 @@ mla_status mla_append(const mla_config* cfg, const void* c_kv_raw, const void* k
 
 size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len) {
   if (check_config(cfg) != MLA_OK || batch < 1) return 0;
+  if (tc_supported(cfg)) return tc_plan(batch).bytes;
   return simt_plan(cfg, batch, max_seq_len).bytes;
 }
 
 int32_t mla_decode_path(const mla_config* cfg) {
-  (void)cfg;
-  return 0;
+  if (check_config(cfg) != MLA_OK) return 0;
+  return tc_supported(cfg) ? 1 : 0;
 }
 
 mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
@@ -259,6 +434,9 @@ mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_r
   if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(pool) ||
       !aligned16(out) || !aligned16(workspace))
     return fail(MLA_ERR_INVALID_ARG, "q_nope, q_rope, w_uk, w_uv, pool, out and workspace must be 16-byte aligned");
+  if (tc_supported(cfg))
+    return decode_tc(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
+                     max_seq_len, out, workspace, workspace_bytes, as_stream(stream));
   return decode_simt(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
                      max_seq_len, out, workspace, workspace_bytes, as_stream(stream));
 }
@@ -295,7 +473,7 @@ mla_status mla_check_device_errors(void* stream) {
 }
 
 const char* mla_decode_stage_names(const mla_config* cfg) {
-  (void)cfg;
+  if (cfg && check_config(cfg) == MLA_OK && tc_supported(cfg)) return "absorb_tc,attend_tc,combine_tc";
   return "absorb_simt,attend_simt,combine_simt";
 }
 
