@@ -3,7 +3,7 @@
 // queries and weights, bf16 cache rows of 576 values (DeepSeek-V2 report,
 // section 2.1.2 absorbed form, section 2.1.3 decoupled RoPE).
 //
-// Three kernels per decode:
+// Four kernels per decode:
 //   absorb  : Q_lat[b,i,0:512] = W_UK[i]^T q_nope[b,i] (one CTA per head, the
 //             whole 128 KB weight slice in flight at once, M = 4 x 128 latent
 //             rows, N = batch), q_rope copied to Q_lat[b,i,512:576]; one
@@ -18,9 +18,10 @@
 //             (identical) online softmax, and accumulates its half of O_lat
 //             in TMEM. Each segment ends in an unnormalised partial
 //             (O half, running max m, sum l).
-//   combine : one CTA per head: log-sum-exp merge of the partials of every
-//             sequence, o_lat split into bf16 hi + lo, then
-//             out[b,i,:] = W_UV[i] (o_hi + o_lo) on the tensor cores.
+//   merge   : one warp per (sequence, head): log-sum-exp merge of the
+//             sequence's partials, o_lat written as bf16 hi + lo.
+//   uv      : one CTA per head: out[b,i,:] = W_UV[i] (o_hi + o_lo) on the
+//             tensor cores (M = 128 output rows, N = sequences).
 #pragma once
 
 #include "common.cuh"
@@ -32,11 +33,13 @@ namespace tcd {
 constexpr int kH = 128, kDc = 512, kDr = 64, kDh = 128, kRow = 576;
 constexpr int kTile = 64;                    // tokens per attend tile
 constexpr int kBlk = kTile * 128;            // one TMA box: 64 rows x 64 bf16 (128 B) = 8 KB
-constexpr int kStageBlks = 5;                // CTA0: 4 latent boxes + 1 rope box; CTA1: 4 latent boxes
-constexpr int kStageBytes = kStageBlks * kBlk;
-constexpr int kStages = 4;
-constexpr int kXbufBytes = kH * kTile * 4;   // one partial score tile, fp32
-constexpr int kAttendThreads = 256;          // warp 0 TMA, warp 1 MMA, warps 4-7 softmax/epilogue
+constexpr int kStageBytes = 4 * kBlk;        // latent boxes of one tile for one CTA: 256 columns
+constexpr int kStages = 5;                   // latent ring depth
+constexpr int kRopeStages = 3;               // rope ring depth (CTA0 only)
+constexpr int kXvalBytes = kH * kTile * 2;   // one partial score tile as fp16
+constexpr int kXbufBytes = kXvalBytes + 2 * kH * 4;   // + one power-of-two scale per (row, column half)
+constexpr int kSoftmaxThreads = 256;         // 8 warps: 4 TMEM lane quarters x 2 column halves
+constexpr int kAttendThreads = 128 + kSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 4-11 softmax
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: O is rescaled only when the max grows by > 2^8
 
 // TMEM columns of the attend kernel (512 allocated)
@@ -44,6 +47,20 @@ constexpr uint32_t kTmO = 0;     // O half: 128 lanes x 256 fp32
 constexpr uint32_t kTmS = 256;   // partial / full score tile: 64 fp32
 constexpr uint32_t kTmQ = 320;   // Q slice, bf16 pairs: up to 160 columns
 constexpr uint32_t kTmP = 480;   // probabilities, bf16 pairs: 32 columns
+
+// Layouts in the workspace. Both are chunk-major so that a warp holding 32
+// consecutive heads touches one contiguous 512-byte line:
+//   Q_lat  [B][72 chunks][128 heads][8 bf16]   chunk c = latent 8c..8c+7 (c < 64), rope 8(c-64).. (c >= 64)
+//   part_o [slot][128 chunks][128 heads][4 fp32]  chunk c = latent 4c..4c+3
+constexpr int kQChunks = kRow / 8;    // 72
+constexpr int kOChunks = kDc / 4;     // 128
+
+__host__ __device__ __forceinline__ int64_t qlat_index(int64_t b, int chunk, int head) {
+  return ((b * kQChunks + chunk) * kH + head) * 8;
+}
+__host__ __device__ __forceinline__ int64_t parto_index(int64_t slot, int chunk, int head) {
+  return ((slot * kOChunks + chunk) * kH + head) * 4;
+}
 
 struct Plan {
   int32_t* lens;   // [B] lengths clamped to [0, max_seq_len]
@@ -62,7 +79,7 @@ __host__ __device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, in
 struct AbsorbArgs {
   const uint16_t* q_rope;     // [B, H, 64]
   const int32_t* seq_lens;    // [B]
-  uint16_t* q_lat;            // [B, H, 576]
+  uint16_t* q_lat;            // chunk-major, see qlat_index
   Plan plan;
   int batch, nb, max_seq_len;
 };
@@ -141,11 +158,11 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
     tc::mbar_arrive_expect_tx(&bars[0], 8 * 16384);
     for (int j = 0; j < 8; ++j) tc::tma_load_2d(sA + j * 16384, &map_wuk, 64 * j, i * kDh, &bars[0]);
   }
-  // q_rope -> Q_lat[:, i, 512:576]
+  // q_rope -> Q_lat chunks 64..71 of head i
   for (int idx = threadIdx.x; idx < a.batch * 8; idx += kAbsorbThreads) {
     const int b = idx >> 3, c = idx & 7;
     const uint4 v = reinterpret_cast<const uint4*>(a.q_rope + (static_cast<int64_t>(b) * kH + i) * kDr)[c];
-    reinterpret_cast<uint4*>(a.q_lat + (static_cast<int64_t>(b) * kH + i) * kRow + kDc)[c] = v;
+    *reinterpret_cast<uint4*>(a.q_lat + qlat_index(b, kDc / 8 + c, i)) = v;
   }
   const uint32_t idesc = tc::idesc_bf16_f32(128, a.nb, 1, 0);
   bool ok = true;
@@ -180,9 +197,9 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int b = n0 + c0 + c;
+          const int k = mt * 128 + 32 * warp + lane;   // latent element
           if (b < a.batch && ok)
-            a.q_lat[(static_cast<int64_t>(b) * kH + i) * kRow + mt * 128 + 32 * warp + lane] =
-                f32_to_bf16_bits(__uint_as_float(r[c]));
+            a.q_lat[qlat_index(b, k >> 3, i) + (k & 7)] = f32_to_bf16_bits(__uint_as_float(r[c]));
         }
       }
     }
@@ -194,19 +211,25 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
 
 // ================================================================== attend
 struct AttendArgs {
-  const uint16_t* q_lat;      // [B, H, 576]
+  const uint16_t* q_lat;      // chunk-major, see qlat_index
   const int32_t* block_table; // [B, max_pages] (NULL: contiguous, sequence b owns pages b*max_pages ..)
   Plan plan;
-  float* part_o;              // [slots, H, 512] fp32, unnormalised
+  float* part_o;              // chunk-major (see parto_index) fp32, unnormalised
   float* part_ml;             // [slots, H, 2]: running max (log2 units) and sum
   int64_t num_pages;
   int batch, max_pages, page_size;
-  float scale_log2;
+  float scale_log2;           // softmax scale * log2(e), > 0
 };
 
 struct AttendSmem {
-  uint64_t full[kStages], empty[kStages];
-  uint64_t s_full, s_free, p_full, o_done, q_ready, o_free, xfull, xempty, drain;
+  uint64_t full[kStages], empty[kStages];       // latent ring
+  uint64_t rfull[kRopeStages], rempty[kRopeStages];  // rope ring (CTA0)
+  uint64_t s_full, s_free, p_full, o_done, q_ready, o_free, drain;
+  uint64_t xfull[2];          // peer partial scores landed in xbuf[0/1] (byte-counted)
+  uint64_t pair_max[4][2];    // the two softmax warps of a lane quarter swapped row maxima (by tile parity)
+  uint64_t pair_sum[4];       // ... and row sums at a segment end
+  float red[2][2][kH];        // per-half row maxima, by tile parity, shared by the two softmax halves
+  float redl[2][kH];          // per-half row sums at a segment end
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -233,7 +256,6 @@ __device__ __forceinline__ SegIter seg_begin(const int32_t* cum, int batch, uint
   SegIter it;
   it.t = share_begin(c, T, nc);
   it.t1 = share_begin(c + 1, T, nc);
-  // first sequence whose tiles reach past t: binary search on cum
   int lo = 0, hi = batch;  // cum[lo] <= t < cum[hi] when t < T
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -251,36 +273,114 @@ __device__ __forceinline__ void set_abort(AttendSmem* s) {
   *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1;
 }
 
+// Score MMAs over NK steps of 16 along the contraction, B = NK/4 boxes of 8 KB
+// from b0; unrolled so that no branch separates two MMAs. `first` = 1 starts
+// the accumulation.
+template <int NK>
+__device__ __forceinline__ void issue_scores(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc, uint32_t first) {
+#pragma unroll
+  for (int k = 0; k < NK; ++k)
+    tc::mma_ts(d, a + 8 * k, b0 + static_cast<uint64_t>(((k >> 2) * kBlk + (k & 3) * 32) >> 4), idesc,
+               (k == 0 && first) ? 0u : 1u);
+}
+
+// O half [128 heads x 256] (+)= P (TMEM, 64 tokens) x V (the tile's 4 latent boxes, MN-major).
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t b0, uint32_t idesc, uint32_t acc0) {
+  tc::mma_ts(d, a, b0, idesc, acc0);
+#pragma unroll
+  for (int k = 1; k < 4; ++k) tc::mma_ts(d, a + 8 * k, b0 + static_cast<uint64_t>((k * 2048) >> 4), idesc, 1u);
+}
+
+// This half's share of the Q slice of sequence b (row h) into TMEM columns
+// kTmQ.. as bf16 pairs. CTA0's slice is latent 0..255 then rope 512..575
+// (40 chunks of 16 bytes), CTA1's latent 256..511 (32 chunks); half 0 takes
+// the first half of the chunks.
+template <int NCH>
+__device__ __forceinline__ void load_q_half(const uint16_t* q_lat, int b, int h, uint32_t rank, int half,
+                                            uint32_t taddr) {
+  constexpr int kHalf = NCH / 2;
+  uint4 v[kHalf];
+#pragma unroll
+  for (int u = 0; u < kHalf; ++u) {
+    const int c = half * kHalf + u;   // chunk of this CTA's slice
+    const int qc = rank == 0 ? (c < 32 ? c : kDc / 8 + (c - 32)) : 32 + c;
+    v[u] = *reinterpret_cast<const uint4*>(q_lat + qlat_index(b, qc, h));
+  }
+#pragma unroll
+  for (int u = 0; u < kHalf; u += 4) {
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      w[4 * e] = v[u + e].x; w[4 * e + 1] = v[u + e].y; w[4 * e + 2] = v[u + e].z; w[4 * e + 3] = v[u + e].w;
+    }
+    tc::tmem_st16(taddr + 4 * (half * kHalf + u), w);
+  }
+  tc::tmem_st_wait();
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))); }
+__device__ __forceinline__ float f16_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }
+
+// Partial scores travel between the two CTAs as fp16 scaled by 2^-k, with k
+// chosen per (row, column half) so that the largest magnitude stays below
+// 2^15: no overflow whatever the inputs, 11 significant bits. Both CTAs add
+// the same rounded values, so their softmax decisions agree bit for bit.
+__device__ __forceinline__ float exchange_scale(float amax, float* unscale) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+  const int k = e > 14 ? e - 14 : 0;
+  *unscale = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+  return __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     attend_tc_kernel(const __grid_constant__ CUtensorMap map_pool, AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* tiles = sm;
-  float* xbuf = reinterpret_cast<float*>(sm + kStages * kStageBytes);
-  AttendSmem* S = reinterpret_cast<AttendSmem*>(sm + kStages * kStageBytes + kXbufBytes);
+  uint8_t* tiles = sm;                                           // kStages x 32 KB latent boxes
+  uint8_t* ropes = sm + kStages * kStageBytes;                   // kRopeStages x 8 KB (CTA0)
+  uint8_t* xbuf = ropes + kRopeStages * kBlk;                    // 2 x [128 heads x 64] bf16
+  AttendSmem* S = reinterpret_cast<AttendSmem*>(xbuf + 2 * kXbufBytes);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
   const uint32_t cl = tc::cluster_id_x(), ncl = tc::n_clusters_x();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_blk = rank == 0 ? 5 : 4;          // boxes per tile for this CTA
-  const int n_k = n_blk * 4;                    // K steps of 16 in the score MMA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&S->full[s], 1);
       tc::mbar_init(&S->empty[s], 1);
     }
+    for (int s = 0; s < kRopeStages; ++s) {
+      tc::mbar_init(&S->rfull[s], 1);
+      tc::mbar_init(&S->rempty[s], 1);
+    }
     tc::mbar_init(&S->s_full, 1);
-    tc::mbar_init(&S->s_free, 128);
-    tc::mbar_init(&S->p_full, 128);
+    tc::mbar_init(&S->s_free, kSoftmaxThreads);
+    tc::mbar_init(&S->p_full, kSoftmaxThreads);
     tc::mbar_init(&S->o_done, 1);
-    tc::mbar_init(&S->q_ready, 128);
-    tc::mbar_init(&S->o_free, 128);
-    tc::mbar_init(&S->xfull, 128);
-    tc::mbar_init(&S->xempty, 128);
+    tc::mbar_init(&S->q_ready, kSoftmaxThreads);
+    tc::mbar_init(&S->o_free, kSoftmaxThreads);
     tc::mbar_init(&S->drain, 1);
+    tc::mbar_init(&S->xfull[0], 1);
+    tc::mbar_init(&S->xfull[1], 1);
+    for (int q = 0; q < 4; ++q) {
+      tc::mbar_init(&S->pair_max[q][0], 64);
+      tc::mbar_init(&S->pair_max[q][1], 64);
+      tc::mbar_init(&S->pair_sum[q], 64);
+    }
     S->abort_flag = 0;
     tc::fence_mbar_init();
+    // both exchange buffers expect one partial score tile from the peer
+    tc::mbar_arrive_expect_tx(&S->xfull[0], kXbufBytes);
+    tc::mbar_arrive_expect_tx(&S->xfull[1], kXbufBytes);
     tc::tma_prefetch_map(&map_pool);
   }
   if (warp == 1) tc::tmem_alloc<512>(&S->tmem_base);
@@ -293,92 +393,139 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
   const int32_t* cum = a.plan.cum;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      const uint64_t policy = tc::policy_evict_first();
-      SegIter si = seg_begin(cum, a.batch, cl, ncl);
-      int b, j0, j1;
-      uint32_t it = 0;
-      bool ok = true;
-      while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
-        for (int j = j0; j < j1 && ok; ++j, ++it) {
-          const int st = it % kStages;
-          if (it >= kStages) ok = tc::mbar_wait(&S->empty[st], ((it / kStages) - 1) & 1);
-          if (!ok || aborted(S)) { ok = false; break; }
-          const int64_t tok = static_cast<int64_t>(j) * kTile;
+    // ---------------------------------------------------------------- TMA producer (whole warp walks
+    // the tiles; lane l looks up the page of the l-th tile of each group of 32, lane 0 issues)
+    const uint64_t policy = tc::policy_evict_first();
+    SegIter si = seg_begin(cum, a.batch, cl, ncl);
+    int b, j0, j1;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+      for (int jc = j0; jc < j1 && ok; jc += 32) {
+        int32_t y_l = 0;
+        const int jl = jc + lane;
+        if (jl < j1) {
+          const int64_t tok = static_cast<int64_t>(jl) * kTile;
           const int pg = static_cast<int>(tok / a.page_size);
           int64_t page = -1;
           if (pg < a.max_pages)
             page = a.block_table ? a.block_table[static_cast<int64_t>(b) * a.max_pages + pg]
                                  : static_cast<int64_t>(b) * a.max_pages + pg;
-          int32_t y;
           if (page < 0 || page >= a.num_pages) {
             flag_error(ERR_BIT_BOUNDS);
-            y = -2 * kTile;  // entirely outside the pool: the copy fills zeros
+            y_l = -2 * kTile;  // entirely outside the pool: the copy fills zeros
           } else {
-            y = static_cast<int32_t>(page * a.page_size + tok % a.page_size);
+            y_l = static_cast<int32_t>(page * a.page_size + tok % a.page_size);
           }
-          uint8_t* dst = tiles + st * kStageBytes;
-          tc::mbar_arrive_expect_tx(&S->full[st], n_blk * kBlk);
-          for (int k = 0; k < 4; ++k)
-            tc::tma_load_2d_hint(dst + k * kBlk, &map_pool, static_cast<int>(rank) * 256 + 64 * k, y, &S->full[st],
-                                 policy);
-          if (rank == 0) tc::tma_load_2d_hint(dst + 4 * kBlk, &map_pool, kDc, y, &S->full[st], policy);
+        }
+        const int n = min(32, j1 - jc);
+        for (int u = 0; u < n; ++u) {
+          const int32_t y = __shfl_sync(0xffffffffu, y_l, u);
+          if (lane == 0 && ok) {
+            const int st = it % kStages, rs = it % kRopeStages;
+            if (it >= kStages) ok = tc::mbar_wait(&S->empty[st], ((it / kStages) - 1) & 1);
+            if (ok && rank == 0 && it >= kRopeStages) ok = tc::mbar_wait(&S->rempty[rs], ((it / kRopeStages) - 1) & 1);
+            if (ok && aborted(S)) ok = false;
+            if (ok) {
+              uint8_t* dst = tiles + st * kStageBytes;
+              tc::mbar_arrive_expect_tx(&S->full[st], kStageBytes);
+              for (int k = 0; k < 4; ++k)
+                tc::tma_load_2d_hint(dst + k * kBlk, &map_pool, static_cast<int>(rank) * 256 + 64 * k, y,
+                                     &S->full[st], policy);
+              if (rank == 0) {
+                tc::mbar_arrive_expect_tx(&S->rfull[rs], kBlk);
+                tc::tma_load_2d_hint(ropes + rs * kBlk, &map_pool, kDc, y, &S->rfull[rs], policy);
+              }
+              ++it;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
         }
       }
+    }
+    it = __shfl_sync(0xffffffffu, it, 0);
+    if (lane == 0) {
       if (!ok) set_abort(S);
       // drain: copies still in flight must land before the CTA exits
       const uint32_t first = it > kStages ? it - kStages : 0;
       for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kStages], (q / kStages) & 1);
+      if (rank == 0) {
+        const uint32_t rfirst = it > kRopeStages ? it - kRopeStages : 0;
+        for (uint32_t q = rfirst; q < it; ++q) tc::mbar_wait(&S->rfull[q % kRopeStages], (q / kRopeStages) & 1);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // Order: S(it), then PV(it-2): the scores of the next tile never wait for
+    // the softmax of the previous one. Every signal the softmax warps give
+    // while working on segment k comes after the epilogue of segment k-1,
+    // which needs all PVs of that segment: before waiting on such a signal,
+    // the PVs of all older segments are issued (flush_before).
     if (lane == 0) {
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kTile, 0, 0);
       const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+      const uint64_t desc0 = tc::sdesc_sw128(tc::smem_u32(tiles), 16, 1024);      // K-major tile, stage 0
+      const uint64_t rdesc0 = tc::sdesc_sw128(tc::smem_u32(ropes), 16, 1024);     // K-major rope box, stage 0
+      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(tiles), kBlk, 1024);   // MN-major V, stage 0
       SegIter si = seg_begin(cum, a.batch, cl, ncl);
       int b, j0, j1;
       uint32_t it = 0, seg = 0;
       bool ok = true;
-      // lagged PV of the previous tile
-      bool have_prev = false, prev_first = false;
-      uint32_t prev_stage = 0, prev_seg = 0;
-      auto issue_pv = [&](uint32_t q) -> bool {
+      // tiles whose PV is still to be issued, oldest first
+      uint32_t pq_it[3] = {0, 0, 0}, pq_first[3] = {0, 0, 0}, pq_seg[3] = {0, 0, 0};
+      uint32_t pend_n = 0;
+      auto pv_oldest = [&]() -> bool {
+        const uint32_t q = pq_it[0], first = pq_first[0], sg = pq_seg[0];
         if (!tc::mbar_wait(&S->p_full, q & 1)) return false;
-        if (prev_first && prev_seg > 0 && !tc::mbar_wait(&S->o_free, (prev_seg - 1) & 1)) return false;
+        if (first && sg > 0 && !tc::mbar_wait(&S->o_free, (sg - 1) & 1)) return false;
         tc::tc_fence_after();
-        const uint32_t base = tc::smem_u32(tiles + prev_stage * kStageBytes);
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t bd = tc::sdesc_sw128(base + k * 2048, kBlk, 1024);
-          tc::mma_ts(tm + kTmO, tm + kTmP + 8 * k, bd, idesc_o, (k > 0 || !prev_first) ? 1u : 0u);
-        }
+        const uint32_t st = q % kStages;
+        issue_pv(tm + kTmO, tm + kTmP, vdesc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_o,
+                 first ? 0u : 1u);
         tc::mma_commit(&S->o_done);
-        tc::mma_commit(&S->empty[prev_stage]);
+        tc::mma_commit(&S->empty[st]);
+        pq_it[0] = pq_it[1]; pq_first[0] = pq_first[1]; pq_seg[0] = pq_seg[1];
+        pq_it[1] = pq_it[2]; pq_first[1] = pq_first[2]; pq_seg[1] = pq_seg[2];
+        --pend_n;
         return true;
       };
+      auto flush_before = [&](uint32_t sg) -> bool {   // issue pending PVs of segments < sg
+        bool good = true;
+        while (good && pend_n > 0 && pq_seg[0] < sg) good = pv_oldest();
+        return good;
+      };
+      uint32_t prev_seg = 0;   // segment of tile it-1
       while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
-        ok = tc::mbar_wait(&S->q_ready, seg & 1);
+        // q_ready of segment `seg` comes from the last tile of segment seg-1
+        if (seg >= 2) ok = flush_before(seg - 1);
+        if (ok) ok = tc::mbar_wait(&S->q_ready, seg & 1);
         for (int j = j0; j < j1 && ok; ++j, ++it) {
-          const uint32_t st = it % kStages;
+          const uint32_t st = it % kStages, rs = it % kRopeStages;
           ok = tc::mbar_wait(&S->full[st], (it / kStages) & 1);
-          if (ok && it > 0) ok = tc::mbar_wait(&S->s_free, (it - 1) & 1);
+          if (ok && rank == 0) ok = tc::mbar_wait(&S->rfull[rs], (it / kRopeStages) & 1);
+          if (ok && it > 0) {
+            ok = flush_before(prev_seg);   // s_free(it-1) comes from tile it-1's segment
+            if (ok) ok = tc::mbar_wait(&S->s_free, (it - 1) & 1);
+          }
           if (!ok || aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
-          const uint32_t base = tc::smem_u32(tiles + st * kStageBytes);
-          for (int k = 0; k < n_k; ++k) {
-            const uint64_t bd = tc::sdesc_sw128(base + (k >> 2) * kBlk + (k & 3) * 32, 16, 1024);
-            tc::mma_ts(tm + kTmS, tm + kTmQ + 8 * k, bd, idesc_s, k > 0 ? 1u : 0u);
+          issue_scores<16>(tm + kTmS, tm + kTmQ, desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_s, 1u);
+          if (rank == 0) {
+            issue_scores<4>(tm + kTmS, tm + kTmQ + 128, rdesc0 + static_cast<uint64_t>((rs * kBlk) >> 4), idesc_s, 0u);
+            tc::mma_commit(&S->rempty[rs]);
           }
           tc::mma_commit(&S->s_full);
-          if (have_prev) ok = issue_pv(it - 1);
-          have_prev = true;
-          prev_first = (j == j0);
-          prev_stage = st;
+          pq_it[pend_n] = it;
+          pq_first[pend_n] = (j == j0) ? 1u : 0u;
+          pq_seg[pend_n] = seg;
+          ++pend_n;
           prev_seg = seg;
+          if (pend_n == 3) ok = pv_oldest();
         }
         ++seg;
       }
-      if (ok && have_prev) ok = issue_pv(it - 1);
+      while (ok && pend_n > 0) ok = pv_oldest();
       if (!ok) set_abort(S);
       // every MMA issued so far must complete before TMEM is released
       tc::mma_commit(&S->drain);
@@ -386,163 +533,236 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int h = threadIdx.x - 128;             // head = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int q_words = n_blk * 32;              // bf16 pairs of this CTA's Q slice
-    auto load_q = [&](int b) {
-      const uint16_t* q = a.q_lat + (static_cast<int64_t>(b) * kH + h) * kRow;
-      for (int w0 = 0; w0 < q_words; w0 += 16) {
-        // words w0..w0+15 = K elements 2*w0 .. 2*w0+31
-        const int k0 = 2 * w0;
-        const int col = rank == 0 ? (k0 < 256 ? k0 : kDc + (k0 - 256)) : 256 + k0;
-        const uint4* src = reinterpret_cast<const uint4*>(q + col);
-        uint32_t v[16];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 x = src[u];
-          v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-        }
-        tc::tmem_st16(tm + lane_base + kTmQ + w0, v);
-      }
-      tc::tmem_st_wait();
+    // 8 warps: warp w holds head rows 32 (w % 4) .. +31 (its TMEM lane quarter)
+    // and token columns 32 * half .. +31 of every tile.
+    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    const int h = 32 * quarter + lane;           // head = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    const uint32_t t_s = tm + lane_base + kTmS + 32 * half;
+    const uint32_t t_o = tm + lane_base + kTmO + 128 * half;
+    const uint32_t t_p = tm + lane_base + kTmP + 16 * half;
+    auto load_q = [&](int bq) {
+      if (rank == 0) load_q_half<40>(a.q_lat, bq, h, rank, half, tm + lane_base + kTmQ);
+      else load_q_half<32>(a.q_lat, bq, h, rank, half, tm + lane_base + kTmQ);
       tc::tc_fence_before();
       tc::mbar_arrive(&S->q_ready);
     };
+    // this thread's 64 bytes of row h in the exchange buffers (16-byte chunks 4*half .. +3, swizzled)
+    auto xoff = [&](int q) { return h * 128 + (((4 * half + q) ^ (h & 7)) << 4); };
+    const uint32_t peer_x = tc::map_peer(xbuf, peer);
+    const uint32_t peer_bar0 = tc::map_peer(&S->xfull[0], peer);
+    const uint32_t peer_bar1 = tc::map_peer(&S->xfull[1], peer);
+    const float sl = a.scale_log2;
 
     SegIter si = seg_begin(cum, a.batch, cl, ncl);
     int b, j0, j1;
-    uint32_t it = 0, seg = 0;
+    uint32_t it = 0;
     bool ok = true;
     bool have = si.next(cum, a.batch, &b, &j0, &j1);
     if (have) load_q(b);
+    // the tile waiting for its peer half: its own partial scores as bf16 pairs
+    uint32_t pend[16];
+    float pend_un = 1.f;
+    bool have_pend = false;
+    int pend_valid = 0;
+    uint32_t pend_it = 0;
+    float m_used = -INFINITY, l = 0.f;
+    uint32_t n_epi = 0;   // segment epilogues done (phase of pair_sum)
+
+    // Finishes tile `q`: full scores, online softmax, P to TMEM.
+    auto finish = [&](uint32_t q, int valid) -> bool {
+      const uint32_t xb = q & 1u;
+      if (!tc::mbar_wait(&S->xfull[xb], (q >> 1) & 1)) return false;
+      if (h == 0 && half == 0) tc::mbar_arrive_expect_tx(&S->xfull[xb], kXbufBytes);   // arm its next use
+      float s[32];
+      {
+        const uint8_t* xr = xbuf + xb * kXbufBytes;
+        const float pun = reinterpret_cast<const float*>(xr + kXvalBytes)[half * kH + h];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + xoff(u));
+          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t ow = pend[4 * u + e];
+            s[8 * u + 2 * e] = f16_lo(ow) * pend_un + f16_lo(pw[e]) * pun;
+            s[8 * u + 2 * e + 1] = f16_hi(ow) * pend_un + f16_hi(pw[e]) * pun;
+          }
+        }
+      }
+      const int vh = valid - 32 * half;          // valid columns of this half
+      if (vh < 32) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) if (c >= vh) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 32; ++c) mx = fmaxf(mx, s[c]);
+      S->red[q & 1][half][h] = mx;
+      tc::mbar_arrive(&S->pair_max[quarter][q & 1]);
+      if (!tc::mbar_wait(&S->pair_max[quarter][q & 1], (q >> 1) & 1)) return false;
+      mx = fmaxf(mx, S->red[q & 1][half ^ 1][h]) * sl;
+      bool rescale = false;
+      float alpha = 1.f;
+      if (m_used == -INFINITY) {
+        m_used = mx;
+      } else if (mx > m_used + kRescaleThreshold) {
+        alpha = tc::ex2_approx(m_used - mx);
+        l *= alpha;
+        m_used = mx;
+        rescale = true;
+      }
+      const float neg_m = -m_used;
+      uint32_t p[16];
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const uint32_t w = tc::pack_bf16(tc::ex2_approx(fmaf(s[c], sl, neg_m)), tc::ex2_approx(fmaf(s[c + 1], sl, neg_m)));
+        p[c / 2] = w;
+        psum += bf_lo(w) + bf_hi(w);
+      }
+      l += psum;
+      // PV of the previous tile must be done: the P buffer and O are ours
+      if (q > 0 && !tc::mbar_wait(&S->o_done, (q - 1) & 1)) return false;
+      tc::tc_fence_after();
+      if (rescale) {
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(t_o + c0, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
+          tc::tmem_st16(t_o + c0, r);
+        }
+      }
+      tc::tmem_st16(t_p, p);
+      tc::tmem_st_wait();
+      // rows past the sequence end must not reach PV as NaN/Inf garbage
+      if (valid < kTile) {
+        uint8_t* stage = tiles + (q % kStages) * kStageBytes;
+        const int nrow = kTile - valid;
+        for (int idx = threadIdx.x - 128; idx < nrow * 4 * 8; idx += kSoftmaxThreads) {
+          const int blk = idx / (nrow * 8), rem = idx % (nrow * 8);
+          const int row = valid + rem / 8, ch = rem % 8;
+          *reinterpret_cast<uint4*>(stage + blk * kBlk + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_proxy_async_smem();
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&S->p_full);
+      return true;
+    };
+
     while (ok && have) {
       const int L = a.plan.lens[b];
       const int slot = b + static_cast<int>(cl);
       int nb_, nj0, nj1;
       SegIter si_next = si;
       const bool have_next = si_next.next(cum, a.batch, &nb_, &nj0, &nj1);
-      float m_used = -INFINITY, l = 0.f;
+      m_used = -INFINITY;
+      l = 0.f;
       for (int j = j0; j < j1 && ok; ++j, ++it) {
-        // ---- own partial scores
+        // ---- own partial scores of tile it -> bf16 -> the peer
         ok = tc::mbar_wait(&S->s_full, it & 1);
         if (!ok || aborted(S)) { ok = false; break; }
         tc::tc_fence_after();
-        float s[kTile];
-#pragma unroll
-        for (int c0 = 0; c0 < kTile; c0 += 16) {
-          uint32_t r[16];
-          tc::tmem_ld16(tm + lane_base + kTmS + c0, r);
+        uint32_t own[16];
+        float own_un;
+        {
+          uint32_t r0[16], r1[16];
+          tc::tmem_ld16(t_s, r0);
+          tc::tmem_ld16(t_s + 16, r1);
           tc::tmem_ld_wait();
+          // columns past the sequence end hold scores of whatever the pool rows contain:
+          // zero them so they cannot set the scale (the softmax masks them anyway)
+          const int vh = min(kTile, L - j * kTile) - 32 * half;
+          if (vh < 32) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) s[c0 + c] = __uint_as_float(r[c]);
+            for (int c = 0; c < 16; ++c) {
+              if (c >= vh) r0[c] = 0u;
+              if (16 + c >= vh) r1[c] = 0u;
+            }
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(r0[c])), fabsf(__uint_as_float(r1[c]))));
+          const float sc = exchange_scale(amax, &own_un);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            own[c] = pack_f16(__uint_as_float(r0[2 * c]) * sc, __uint_as_float(r0[2 * c + 1]) * sc);
+            own[8 + c] = pack_f16(__uint_as_float(r1[2 * c]) * sc, __uint_as_float(r1[2 * c + 1]) * sc);
+          }
         }
         tc::tc_fence_before();
         tc::mbar_arrive(&S->s_free);
-        if (j == j1 - 1 && have_next) load_q(nb_);   // all score MMAs of this segment are done
-        // ---- swap partial scores with the peer CTA
-        if (it > 0) ok = tc::mbar_wait<true>(&S->xempty, (it - 1) & 1);
-        if (!ok) break;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int chunk = q ^ (h & 15);
-          tc::st_cluster_v4(tc::map_peer(xbuf + h * kTile + chunk * 4, peer), __float_as_uint(s[4 * q]),
-                            __float_as_uint(s[4 * q + 1]), __float_as_uint(s[4 * q + 2]),
-                            __float_as_uint(s[4 * q + 3]));
-        }
-        tc::mbar_arrive_remote(&S->xfull, peer);
-        ok = tc::mbar_wait<true>(&S->xfull, it & 1);
-        if (!ok) break;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int chunk = q ^ (h & 15);
-          const float4 v = *reinterpret_cast<const float4*>(xbuf + h * kTile + chunk * 4);
-          s[4 * q] += v.x; s[4 * q + 1] += v.y; s[4 * q + 2] += v.z; s[4 * q + 3] += v.w;
-        }
-        tc::mbar_arrive_remote(&S->xempty, peer);
-        // ---- online softmax (base 2), identical in both CTAs
-        const int valid = min(kTile, L - j * kTile);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          s[c] = c < valid ? s[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-        bool rescale = false;
-        float alpha = 1.f;
-        if (m_used == -INFINITY) {
-          m_used = mx;
-        } else if (mx > m_used + kRescaleThreshold) {
-          alpha = exp2f(m_used - mx);
-          l *= alpha;
-          m_used = mx;
-          rescale = true;
-        }
-        uint32_t p[kTile / 2];
-        float psum = 0.f;
-#pragma unroll
-        for (int c = 0; c < kTile; c += 2) {
-          const uint32_t w = tc::pack_bf16(exp2f(s[c] - m_used), exp2f(s[c + 1] - m_used));
-          p[c / 2] = w;
-          psum += bf16_to_f32(static_cast<uint16_t>(w & 0xffffu)) + bf16_to_f32(static_cast<uint16_t>(w >> 16));
-        }
-        l += psum;
-        // ---- PV of the previous tile must be done: P buffer and O are ours
-        if (it > 0) ok = tc::mbar_wait(&S->o_done, (it - 1) & 1);
-        if (!ok) break;
-        tc::tc_fence_after();
-        if (rescale) {
-          for (int c0 = 0; c0 < 256; c0 += 16) {
-            uint32_t r[16];
-            tc::tmem_ld16(tm + lane_base + kTmO + c0, r);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tc::tmem_st16(tm + lane_base + kTmO + c0, r);
-          }
+        // ---- finish the previous tile of this segment (its peer half arrived while
+        // this tile's scores were computed), then send this tile's half. Sending
+        // only after consuming the peer's previous tile keeps two buffers safe:
+        // the peer sent that tile after it had read what this CTA sent two tiles ago.
+        if (have_pend) {
+          ok = finish(pend_it, pend_valid);
+          if (!ok) break;
         }
         {
-          uint32_t w0[16], w1[16];
+          const uint32_t xb = it & 1u;
+          const uint32_t dst = peer_x + xb * kXbufBytes;
+          const uint32_t bar = xb ? peer_bar1 : peer_bar0;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) { w0[c] = p[c]; w1[c] = p[16 + c]; }
-          tc::tmem_st16(tm + lane_base + kTmP, w0);
-          tc::tmem_st16(tm + lane_base + kTmP + 16, w1);
+          for (int u = 0; u < 4; ++u)
+            tc::st_async_v4(dst + xoff(u), bar, own[4 * u], own[4 * u + 1], own[4 * u + 2], own[4 * u + 3]);
+          tc::st_async_b32(dst + kXvalBytes + 4 * (half * kH + h), bar, __float_as_uint(own_un));
         }
-        tc::tmem_st_wait();
-        // ---- rows past the sequence end must not reach PV as NaN/Inf garbage
-        if (valid < kTile) {
-          uint8_t* stage = tiles + (it % kStages) * kStageBytes;
-          const int nrow = kTile - valid;
-          for (int idx = h; idx < nrow * 4 * 8; idx += 128) {
-            const int blk = idx / (nrow * 8), rem = idx % (nrow * 8);
-            const int row = valid + rem / 8, ch = rem % 8;
-            *reinterpret_cast<uint4*>(stage + blk * kBlk + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-          }
-          tc::fence_proxy_async_smem();
-        }
-        tc::tc_fence_before();
-        tc::mbar_arrive(&S->p_full);
+        if (j == j1 - 1 && have_next) load_q(nb_);   // all score MMAs of this segment are done
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pend[c] = own[c];
+        pend_un = own_un;
+        pend_valid = min(kTile, L - j * kTile);
+        pend_it = it;
+        have_pend = true;
       }
+      if (!ok) break;
+      ok = finish(pend_it, pend_valid);
+      have_pend = false;
       if (!ok) break;
       // ---- segment epilogue: unnormalised O half, m and l
       ok = tc::mbar_wait(&S->o_done, (it - 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
-      float* dst = a.part_o + (static_cast<int64_t>(slot) * kH + h) * kDc + rank * 256;
-      for (int c0 = 0; c0 < 256; c0 += 16) {
-        uint32_t r[16];
-        tc::tmem_ld16(tm + lane_base + kTmO + c0, r);
+      const int chunk0 = (rank * 256 + 128 * half) / 4;   // first 4-float chunk of this thread's columns
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 64) {
+        uint32_t r0[16], r1[16], r2[16], r3[16];
+        tc::tmem_ld16(t_o + c0, r0);
+        tc::tmem_ld16(t_o + c0 + 16, r1);
+        tc::tmem_ld16(t_o + c0 + 32, r2);
+        tc::tmem_ld16(t_o + c0 + 48, r3);
         tc::tmem_ld_wait();
+        const int ch = chunk0 + c0 / 4;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          reinterpret_cast<uint4*>(dst + c0)[u] = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) {
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + u, h)) =
+              make_uint4(r0[4 * u], r0[4 * u + 1], r0[4 * u + 2], r0[4 * u + 3]);
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + 4 + u, h)) =
+              make_uint4(r1[4 * u], r1[4 * u + 1], r1[4 * u + 2], r1[4 * u + 3]);
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + 8 + u, h)) =
+              make_uint4(r2[4 * u], r2[4 * u + 1], r2[4 * u + 2], r2[4 * u + 3]);
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + 12 + u, h)) =
+              make_uint4(r3[4 * u], r3[4 * u + 1], r3[4 * u + 2], r3[4 * u + 3]);
+        }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&S->o_free);
-      if (rank == 0) {
+      // l of the two halves (both scaled by the same factors)
+      S->redl[half][h] = l;
+      tc::mbar_arrive(&S->pair_sum[quarter]);
+      ok = tc::mbar_wait(&S->pair_sum[quarter], n_epi & 1);
+      ++n_epi;
+      if (!ok) break;
+      if (rank == 0 && half == 0) {
         float2* ml = reinterpret_cast<float2*>(a.part_ml) + static_cast<int64_t>(slot) * kH + h;
-        *ml = make_float2(m_used, l);
+        *ml = make_float2(m_used, l + S->redl[1][h]);
       }
-      ++seg;
       have = si.next(cum, a.batch, &b, &j0, &j1);
     }
     if (!ok) set_abort(S);
@@ -557,42 +777,116 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
   if (warp == 1) tc::tmem_dealloc<512>(tm);
 }
 
-// ================================================================== combine + W_UV
-struct CombineArgs {
+// ================================================================== merge (log-sum-exp over segments)
+struct MergeArgs {
   Plan plan;
-  const float* part_o;
-  const float* part_ml;
-  float* out;          // [B, H, 128]
+  const float* part_o;   // chunk-major, see parto_index
+  const float* part_ml;  // [slots, H, 2]
+  uint16_t* o_hi;        // [B, H, 512] bf16: o_lat rounded
+  uint16_t* o_lo;        // [B, H, 512] bf16: o_lat - o_hi rounded
   int batch, ncl;
 };
 
-constexpr int kCombineThreads = 128;
-constexpr int kCombineNb = 32;        // sequences per MMA chunk
-constexpr int kCombineMaxSlots = 512; // partial slots one chunk may touch: kCombineNb + clusters
+constexpr int kMergeChunks = 4;                  // 4-float chunks per CTA (16 latent elements)
+constexpr int kMergeSplit = kOChunks / kMergeChunks;   // CTAs per sequence
 
-// Dynamic shared memory of the combine kernel (after 1 KB alignment).
-constexpr size_t kCombineSmem = 8 * 16384 + 2 * 8 * kCombineNb * 128 + kCombineMaxSlots * 4 + 2 * kCombineNb * 4 + 64;
+// One CTA per (sequence b, 16 latent elements); thread = head. o_lat =
+// sum_s w_s O_s / sum_s w_s l_s with w_s = 2^(m_s - max m) over the partials
+// of b's segments (slots b + c for the clusters c whose shares meet b's
+// tiles). Every load is a warp reading 32 consecutive heads of one chunk.
+__global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int h = threadIdx.x;
+  const int b = blockIdx.y;
+  const int chunk0 = blockIdx.x * kMergeChunks;
+  const int64_t T = a.plan.cum[a.batch];
+  const int64_t tb0 = a.plan.cum[b], tb1 = a.plan.cum[b + 1];
+  float4 acc[kMergeChunks];
+#pragma unroll
+  for (int k = 0; k < kMergeChunks; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (T > 0 && tb1 > tb0) {
+    const int64_t c0 = share_owner(tb0, T, a.ncl), c1 = share_owner(tb1 - 1, T, a.ncl);
+    const float2* ml_all = reinterpret_cast<const float2*>(a.part_ml);
+    // running max and denominator in one pass
+    float M = -INFINITY, den = 0.f;
+    for (int64_t c = c0; c <= c1; ++c) {
+      if (share_begin(c, T, a.ncl) == share_begin(c + 1, T, a.ncl)) continue;   // empty share: no partial
+      const float2 ml = ml_all[(b + c) * kH + h];
+      if (ml.x > M) {
+        den = den * exp2f(M - ml.x) + ml.y;
+        M = ml.x;
+      } else {
+        den += exp2f(ml.x - M) * ml.y;
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll 2
+    for (int64_t c = c0; c <= c1; ++c) {
+      if (share_begin(c, T, a.ncl) == share_begin(c + 1, T, a.ncl)) continue;
+      const float w = exp2f(ml_all[(b + c) * kH + h].x - M) * inv;
+      float4 v[kMergeChunks];
+#pragma unroll
+      for (int k = 0; k < kMergeChunks; ++k)
+        v[k] = *reinterpret_cast<const float4*>(a.part_o + parto_index(b + c, chunk0 + k, h));
+#pragma unroll
+      for (int k = 0; k < kMergeChunks; ++k) {
+        acc[k].x = fmaf(w, v[k].x, acc[k].x);
+        acc[k].y = fmaf(w, v[k].y, acc[k].y);
+        acc[k].z = fmaf(w, v[k].z, acc[k].z);
+        acc[k].w = fmaf(w, v[k].w, acc[k].w);
+      }
+    }
+  }
+  const int64_t row = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * chunk0;
+#pragma unroll
+  for (int k = 0; k < kMergeChunks; k += 2) {
+    const float v[8] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w, acc[k + 1].x, acc[k + 1].y, acc[k + 1].z, acc[k + 1].w};
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
+      lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
+                            v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
+    }
+    *reinterpret_cast<uint4*>(a.o_hi + row + 4 * k) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(a.o_lo + row + 4 * k) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
 
-__global__ void __launch_bounds__(kCombineThreads) combine_tc_kernel(const __grid_constant__ CUtensorMap map_wuv,
-                                                                     CombineArgs a) {
+// ================================================================== W_UV
+struct UvArgs {
+  float* out;      // [B, H, 128]
+  int batch;
+};
+
+constexpr int kUvThreads = 128;
+constexpr int kUvNb = 32;   // sequences per MMA chunk
+constexpr size_t kUvSmem = 8 * 16384 + 2 * 8 * kUvNb * 128 + 64;
+
+// One CTA per head i: out[b, i, :] = W_UV[i] (o_hi[b, i, :] + o_lo[b, i, :]),
+// M = 128 output rows, N = 32 sequences per chunk, K = 512 twice (hi, lo).
+__global__ void __launch_bounds__(kUvThreads) uv_tc_kernel(const __grid_constant__ CUtensorMap map_wuv,
+                                                           const __grid_constant__ CUtensorMap map_hi,
+                                                           const __grid_constant__ CUtensorMap map_lo, UvArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = sm;                                   // W_UV[i]: 8 boxes [128 rows x 64] = 128 KB
-  uint8_t* sHi = sm + 8 * 16384;                      // o_lat hi: 8 blocks [32 rows x 64] = 32 KB
-  uint8_t* sLo = sHi + 8 * kCombineNb * 128;          // o_lat lo
-  float* wts = reinterpret_cast<float*>(sLo + 8 * kCombineNb * 128);   // merge weight per slot of the chunk
-  int32_t* seg_first = reinterpret_cast<int32_t*>(wts + kCombineMaxSlots);
-  int32_t* seg_count = seg_first + kCombineNb;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(seg_count + kCombineNb);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  uint8_t* sA = sm;                                 // W_UV[i]: 8 boxes [128 rows x 64] = 128 KB
+  uint8_t* sHi = sm + 8 * 16384;                    // o_hi rows: 8 boxes [32 rows x 64] = 32 KB
+  uint8_t* sLo = sHi + 8 * kUvNb * 128;             // o_lo rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sLo + 8 * kUvNb * 128);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
   const int i = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   if (t == 0) {
-    tc::mbar_init(&bars[0], 1);
-    tc::mbar_init(&bars[1], 1);
+    tc::mbar_init(&bars[0], 1);   // weights landed
+    tc::mbar_init(&bars[1], 1);   // o_lat rows landed (one phase per chunk)
+    tc::mbar_init(&bars[2], 1);   // MMAs done (one phase per chunk)
     tc::fence_mbar_init();
     tc::tma_prefetch_map(&map_wuv);
-    // the weights do not depend on the attend kernel: start streaming them now
+    tc::tma_prefetch_map(&map_hi);
+    tc::tma_prefetch_map(&map_lo);
+    // the weights do not depend on the kernels before: start streaming them now
     tc::mbar_arrive_expect_tx(&bars[0], 8 * 16384);
     for (int j = 0; j < 8; ++j) tc::tma_load_2d(sA + j * 16384, &map_wuv, 64 * j, i * kDh, &bars[0]);
   }
@@ -602,103 +896,47 @@ __global__ void __launch_bounds__(kCombineThreads) combine_tc_kernel(const __gri
   tc::tc_fence_after();
   const uint32_t tm = *tslot;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t T = a.plan.cum[a.batch];
-  const uint32_t idesc = tc::idesc_bf16_f32(128, kCombineNb, 0, 0);
-  const float2* ml_all = reinterpret_cast<const float2*>(a.part_ml);
+  const uint32_t idesc = tc::idesc_bf16_f32(128, kUvNb, 0, 0);
   bool ok = true;
   int chunk = 0;
-  for (int n0 = 0; n0 < a.batch; n0 += kCombineNb, ++chunk) {
-    // ---- pass 1 (one thread per sequence): merge weights of its partials.
-    // Sequence b's partials sit in slots b + c for the clusters c whose
-    // shares meet its tiles; in a chunk those slots form one contiguous run.
-    const int64_t slot0 = (T > 0 && n0 < a.batch) ? n0 + share_owner(a.plan.cum[n0] < T ? a.plan.cum[n0] : T - 1, T, a.ncl) : 0;
-    if (t < kCombineNb) {
-      const int b = n0 + t;
-      int first = 0, count = 0;
-      if (b < a.batch && T > 0) {
-        const int64_t tb0 = a.plan.cum[b], tb1 = a.plan.cum[b + 1];
-        if (tb1 > tb0) {
-          const int64_t c0 = share_owner(tb0, T, a.ncl), c1 = share_owner(tb1 - 1, T, a.ncl);
-          float M = -INFINITY;
-          for (int64_t c = c0; c <= c1; ++c)
-            if (share_begin(c, T, a.ncl) < share_begin(c + 1, T, a.ncl)) M = fmaxf(M, ml_all[(b + c) * kH + i].x);
-          float den = 0.f;
-          for (int64_t c = c0; c <= c1; ++c) {
-            float w = 0.f;
-            if (share_begin(c, T, a.ncl) < share_begin(c + 1, T, a.ncl)) {
-              const float2 ml = ml_all[(b + c) * kH + i];
-              w = exp2f(ml.x - M);
-              den += w * ml.y;
-            }
-            wts[b + c - slot0] = w;
-          }
-          const float inv = den > 0.f ? 1.f / den : 0.f;
-          for (int64_t c = c0; c <= c1; ++c) wts[b + c - slot0] *= inv;
-          first = static_cast<int>(b + c0 - slot0);
-          count = static_cast<int>(c1 - c0 + 1);
-        }
-      }
-      seg_first[t] = first;
-      seg_count[t] = count;
-    }
-    __syncthreads();
-    // ---- pass 2: o_lat rows, thread t owns latent elements 4t .. 4t+3 of every row
-    for (int n = 0; n < kCombineNb; ++n) {
-      const int first = seg_first[n], count = seg_count[n];
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int u = 0; u < count; ++u) {
-        const float w = wts[first + u];
-        if (w == 0.f) continue;   // a cluster with an empty share wrote nothing into this slot
-        const float4 o = reinterpret_cast<const float4*>(a.part_o + ((slot0 + first + u) * kH + i) * kDc)[t];
-        acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-      }
-      // hi/lo bf16 split into the K-major 128-byte-swizzled B operand: row n, K = 4t..4t+3
-      const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-      uint32_t hi[2], lo[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t hw = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
-        hi[u] = hw;
-        lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hw & 0xffffu)),
-                              v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hw >> 16)));
-      }
-      const int k = 4 * t, kb = k >> 6, kin = k & 63;
-      const int off = kb * (kCombineNb * 128) + n * 128 + ((((kin >> 3) ^ (n & 7)) << 4)) + (kin & 7) * 2;
-      *reinterpret_cast<uint2*>(sHi + off) = make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(sLo + off) = make_uint2(lo[0], lo[1]);
-    }
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
+  for (int n0 = 0; n0 < a.batch; n0 += kUvNb, ++chunk) {
     if (t == 0) {
+      tc::mbar_arrive_expect_tx(&bars[1], 2 * 8 * kUvNb * 128);
+      for (int k = 0; k < 8; ++k) {
+        tc::tma_load_2d(sHi + k * kUvNb * 128, &map_hi, i * kDc + 64 * k, n0, &bars[1]);
+        tc::tma_load_2d(sLo + k * kUvNb * 128, &map_lo, i * kDc + 64 * k, n0, &bars[1]);
+      }
+      ok = tc::mbar_wait(&bars[0], 0) && tc::mbar_wait(&bars[1], chunk & 1);
       tc::tc_fence_after();
-      ok = tc::mbar_wait(&bars[0], 0);
       if (ok) {
+        const uint64_t a0 = tc::sdesc_sw128(tc::smem_u32(sA), 16, 1024);
+        const uint64_t h0 = tc::sdesc_sw128(tc::smem_u32(sHi), 16, 1024);
+        const uint64_t l0 = tc::sdesc_sw128(tc::smem_u32(sLo), 16, 1024);
+#pragma unroll
         for (int kk = 0; kk < 32; ++kk) {
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + (kk >> 2) * 16384 + (kk & 3) * 32), 16, 1024);
-          const uint32_t boff = (kk >> 2) * (kCombineNb * 128) + (kk & 3) * 32;
-          tc::mma_ss(tm, ad, tc::sdesc_sw128(tc::smem_u32(sHi + boff), 16, 1024), idesc, kk > 0);
-          tc::mma_ss(tm, ad, tc::sdesc_sw128(tc::smem_u32(sLo + boff), 16, 1024), idesc, 1);
+          const uint64_t ad = a0 + static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+          const uint64_t bo = static_cast<uint64_t>(((kk >> 2) * (kUvNb * 128) + (kk & 3) * 32) >> 4);
+          tc::mma_ss(tm, ad, h0 + bo, idesc, kk > 0 ? 1u : 0u);
+          tc::mma_ss(tm, ad, l0 + bo, idesc, 1u);
         }
       }
-      tc::mma_commit(&bars[1]);
+      tc::mma_commit(&bars[2]);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&bars[1], chunk & 1) && ok;
+    ok = tc::mbar_wait(&bars[2], chunk & 1) && ok;
     tc::tc_fence_after();
-    for (int c0 = 0; c0 < kCombineNb; c0 += 16) {
-      uint32_t r[16];
-      tc::tmem_ld16(tc::tmem_at(tm, 32 * warp, c0), r);
-      tc::tmem_ld_wait();
+    uint32_t r0[16], r1[16];
+    tc::tmem_ld16(tc::tmem_at(tm, 32 * warp, 0), r0);
+    tc::tmem_ld16(tc::tmem_at(tm, 32 * warp, 16), r1);
+    tc::tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int b = n0 + c0 + c;
-        if (b < a.batch) a.out[(static_cast<int64_t>(b) * kH + i) * kDh + 32 * warp + lane] = __uint_as_float(r[c]);
-      }
+    for (int c = 0; c < 16; ++c) {
+      const int b0 = n0 + c, b1 = n0 + 16 + c;
+      if (b0 < a.batch) a.out[(static_cast<int64_t>(b0) * kH + i) * kDh + 32 * warp + lane] = __uint_as_float(r0[c]);
+      if (b1 < a.batch) a.out[(static_cast<int64_t>(b1) * kH + i) * kDh + 32 * warp + lane] = __uint_as_float(r1[c]);
     }
     tc::tc_fence_before();
-    __syncthreads();   // the B operand, the weights and TMEM are reused by the next chunk
+    __syncthreads();   // the B operand and TMEM are reused by the next chunk
   }
   if (warp == 0) tc::tmem_dealloc<32>(tm);
 }

@@ -163,7 +163,8 @@ mla_status decode_simt(const mla_config* c, const void* q_nope, const void* q_ro
 // and cache, and pages holding whole 64-token tiles.
 bool tc_supported(const mla_config* c) {
   return c->n_heads == tcd::kH && c->d_c == tcd::kDc && c->d_rope == tcd::kDr && c->d_head == tcd::kDh &&
-         c->io_dtype == MLA_DTYPE_BF16 && c->cache_dtype == MLA_DTYPE_BF16 && c->page_size % tcd::kTile == 0;
+         c->io_dtype == MLA_DTYPE_BF16 && c->cache_dtype == MLA_DTYPE_BF16 && c->page_size % tcd::kTile == 0 &&
+         c->scale > 0.f;
 }
 
 // Clusters the workspace is sized for; a launch never uses more.
@@ -171,7 +172,7 @@ constexpr int kMaxClusters = 128;
 
 struct TcPlan {
   int nb, slots;
-  size_t off_qlat, off_lens, off_cum, off_ml, off_o, bytes;
+  size_t off_qlat, off_lens, off_cum, off_ml, off_o, off_hi, off_lo, bytes;
 };
 
 TcPlan tc_plan(int batch) {
@@ -189,12 +190,18 @@ TcPlan tc_plan(int batch) {
   off = align_up(off + static_cast<size_t>(p.slots) * tcd::kH * 8, 256);
   p.off_o = off;
   off = align_up(off + static_cast<size_t>(p.slots) * tcd::kH * tcd::kDc * 4, 256);
+  p.off_hi = off;
+  off = align_up(off + static_cast<size_t>(batch) * tcd::kH * tcd::kDc * 2, 256);
+  p.off_lo = off;
+  off = align_up(off + static_cast<size_t>(batch) * tcd::kH * tcd::kDc * 2, 256);
   p.bytes = off;
   return p;
 }
 
-constexpr size_t kAttendSmem = 1024 + tcd::kStages * tcd::kStageBytes + tcd::kXbufBytes + sizeof(tcd::AttendSmem);
-constexpr size_t kCombineSmem = 1024 + tcd::kCombineSmem;
+constexpr size_t kAttendSmem = 1024 + tcd::kStages * tcd::kStageBytes + tcd::kRopeStages * tcd::kBlk +
+                               2 * tcd::kXbufBytes + sizeof(tcd::AttendSmem);
+static_assert(kAttendSmem <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
+constexpr size_t kUvSmem = 1024 + tcd::kUvSmem;
 size_t absorb_smem(int nb) { return 1024 + 8 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
 
 struct TcDeviceState {
@@ -220,9 +227,9 @@ mla_status tc_device_setup(int* clusters) {
     if ((e = cudaFuncSetAttribute(tcd::attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kAttendSmem))) != cudaSuccess)
       return cuda_fail(e, "attend smem attribute");
-    if ((e = cudaFuncSetAttribute(tcd::combine_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kCombineSmem))) != cudaSuccess)
-      return cuda_fail(e, "combine smem attribute");
+    if ((e = cudaFuncSetAttribute(tcd::uv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kUvSmem))) != cudaSuccess)
+      return cuda_fail(e, "uv smem attribute");
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2 * kMaxClusters);
     lc.blockDim = dim3(tcd::kAttendThreads);
@@ -273,14 +280,20 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   tcd::Plan plan{reinterpret_cast<int32_t*>(ws + p.off_lens), reinterpret_cast<int32_t*>(ws + p.off_cum)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
-  CUtensorMap m_pool, m_wuk, m_wuv, m_qn;
+  CUtensorMap m_pool, m_wuk, m_wuv, m_qn, m_hi, m_lo;
+  uint16_t* o_hi = reinterpret_cast<uint16_t*>(ws + p.off_hi);
+  uint16_t* o_lo = reinterpret_cast<uint16_t*>(ws + p.off_lo);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
   if (!make_map_2d(&m_pool, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, tcd::kTile, SW) ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
       !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
       !make_map_2d(&m_qn, q_nope, BF, tcd::kH * tcd::kDh, static_cast<uint64_t>(batch), tcd::kH * tcd::kDh * 2, 64,
-                   static_cast<uint32_t>(p.nb), SW))
+                   static_cast<uint32_t>(p.nb), SW) ||
+      !make_map_2d(&m_hi, o_hi, BF, tcd::kH * tcd::kDc, static_cast<uint64_t>(batch), tcd::kH * tcd::kDc * 2, 64,
+                   tcd::kUvNb, SW) ||
+      !make_map_2d(&m_lo, o_lo, BF, tcd::kH * tcd::kDc, static_cast<uint64_t>(batch), tcd::kH * tcd::kDc * 2, 64,
+                   tcd::kUvNb, SW))
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled refused a tensor description (or the driver entry point is missing)");
 
   tcd::AbsorbArgs aa{};
@@ -304,13 +317,18 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   ta.page_size = c->page_size;
   ta.scale_log2 = c->scale * 1.4426950408889634f;
 
-  tcd::CombineArgs ca{};
-  ca.plan = plan;
-  ca.part_o = ta.part_o;
-  ca.part_ml = ta.part_ml;
-  ca.out = out;
-  ca.batch = batch;
-  ca.ncl = ncl;
+  tcd::MergeArgs ma{};
+  ma.plan = plan;
+  ma.part_o = ta.part_o;
+  ma.part_ml = ta.part_ml;
+  ma.o_hi = o_hi;
+  ma.o_lo = o_lo;
+  ma.batch = batch;
+  ma.ncl = ncl;
+
+  tcd::UvArgs ua{};
+  ua.out = out;
+  ua.batch = batch;
 
   stage_mark(0, st);
   tcd::absorb_tc_kernel<<<tcd::kH + 1, tcd::kAbsorbThreads, absorb_smem(p.nb), st>>>(m_wuk, m_qn, aa);
@@ -322,11 +340,16 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  kAttendSmem, st, attend_args);
   if (s != MLA_OK) return s;
   stage_mark(2, st);
-  void* combine_args[] = {&m_wuv, &ca};
-  s = launch_pdl(reinterpret_cast<const void*>(tcd::combine_tc_kernel), dim3(tcd::kH), dim3(tcd::kCombineThreads),
-                 kCombineSmem, st, combine_args);
+  void* merge_args[] = {&ma};
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::merge_kernel), dim3(tcd::kMergeSplit, batch), dim3(tcd::kH), 0,
+                 st, merge_args);
   if (s != MLA_OK) return s;
   stage_mark(3, st);
+  void* uv_args[] = {&m_wuv, &m_hi, &m_lo, &ua};
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::uv_tc_kernel), dim3(tcd::kH), dim3(tcd::kUvThreads), kUvSmem, st,
+                 uv_args);
+  if (s != MLA_OK) return s;
+  stage_mark(4, st);
   return MLA_OK;
 }
 
@@ -473,7 +496,7 @@ mla_status mla_check_device_errors(void* stream) {
 }
 
 const char* mla_decode_stage_names(const mla_config* cfg) {
-  if (cfg && check_config(cfg) == MLA_OK && tc_supported(cfg)) return "absorb_tc,attend_tc,combine_tc";
+  if (cfg && check_config(cfg) == MLA_OK && tc_supported(cfg)) return "absorb_tc,attend_tc,merge,uv_tc";
   return "absorb_simt,attend_simt,combine_simt";
 }
 
