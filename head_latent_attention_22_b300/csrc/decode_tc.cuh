@@ -39,7 +39,7 @@ constexpr int kRopeStages = 3;               // rope ring depth (CTA0 only)
 constexpr int kXvalBytes = kH * kTile * 2;   // one partial score tile as fp16
 constexpr int kXbufBytes = kXvalBytes + 2 * kH * 4;   // + one power-of-two scale per (row, column half)
 constexpr int kSoftmaxThreads = 256;         // 8 warps: 4 TMEM lane quarters x 2 column halves
-constexpr int kAttendThreads = 128 + kSoftmaxThreads;  // warp 0 TMA, warp 1 MMA, warps 4-11 softmax
+constexpr int kAttendThreads = 128 + kSoftmaxThreads;  // warp 0 TMA, warps 1-2 MMA, warps 4-11 softmax
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: O is rescaled only when the max grows by > 2^8
 
 // TMEM columns of the attend kernel (512 allocated)
@@ -63,8 +63,12 @@ __host__ __device__ __forceinline__ int64_t parto_index(int64_t slot, int chunk,
 }
 
 struct Plan {
-  int32_t* lens;   // [B] lengths clamped to [0, max_seq_len]
-  int32_t* cum;    // [B+1] prefix sums of ceil(len / 64)
+  int32_t* lens;         // [B] lengths clamped to [0, max_seq_len]
+  int32_t* cum;          // [B+1] prefix sums of ceil(len / 64)
+  int32_t* first_seq;    // [clusters] sequence holding the first tile of each cluster's share
+  int32_t* share_start;  // [clusters + 1] first tile of each cluster's share (share c = [start[c], start[c+1]))
+  int32_t* seq_c0;       // [B] first cluster whose share meets sequence b's tiles (when it has any)
+  int32_t* seq_c1;       // [B] last such cluster
 };
 
 // Tile range [t0, t1) of cluster c when T tiles are split over nc clusters.
@@ -81,7 +85,7 @@ struct AbsorbArgs {
   const int32_t* seq_lens;    // [B]
   uint16_t* q_lat;            // chunk-major, see qlat_index
   Plan plan;
-  int batch, nb, max_seq_len;
+  int batch, nb, max_seq_len, ncl;
 };
 
 constexpr int kAbsorbThreads = 128;
@@ -122,74 +126,109 @@ __device__ void plan_block(const AbsorbArgs& a) {
     if (threadIdx.x == kAbsorbThreads - 1) carry = off + x;
     __syncthreads();
   }
+  // cluster shares: start tile and first sequence of each; clusters of each sequence
+  const int64_t T = a.plan.cum[a.batch];
+  for (int c = threadIdx.x; c <= a.ncl; c += kAbsorbThreads) {
+    const int64_t t = share_begin(c, T, a.ncl);
+    a.plan.share_start[c] = static_cast<int32_t>(t);
+    if (c == a.ncl) continue;
+    int lo = 0, hi = a.batch;   // cum[lo] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (a.plan.cum[mid] <= t) lo = mid; else hi = mid;
+    }
+    a.plan.first_seq[c] = lo;
+  }
+  for (int b = threadIdx.x; b < a.batch; b += kAbsorbThreads) {
+    const int64_t tb0 = a.plan.cum[b], tb1 = a.plan.cum[b + 1];
+    if (tb1 > tb0) {
+      a.plan.seq_c0[b] = static_cast<int32_t>(share_owner(tb0, T, a.ncl));
+      a.plan.seq_c1[b] = static_cast<int32_t>(share_owner(tb1 - 1, T, a.ncl));
+    } else {
+      a.plan.seq_c0[b] = 0;
+      a.plan.seq_c1[b] = -1;
+    }
+  }
 }
 
-// One CTA per head i (blockIdx.x < H); CTA H writes the plan.
+// Two CTAs per head i (blockIdx.x = 2 i + half, half = 128-row M tiles
+// 2 half and 2 half + 1 of the 512 latent rows); the last CTA writes the plan.
+// Each CTA streams its 64 KB of W_UK[i] with one barrier per M tile, so the
+// MMAs of the first tile start while the second is still in flight; the
+// weights are requested before the wait on the preceding kernel.
 __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_constant__ CUtensorMap map_wuk,
                                                                    const __grid_constant__ CUtensorMap map_qn,
                                                                    AbsorbArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == kH) {
+  if (blockIdx.x == 2 * kH) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     plan_block(a);
     return;
   }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = sm;                          // 8 boxes [128 d_h rows x 64 latent] = 128 KB
-  uint8_t* sB = sm + 8 * 16384;              // 2 boxes [nb rows x 64 d_h]
+  uint8_t* sA = sm;                          // 4 boxes [128 d_h rows x 64 latent] = 64 KB
+  uint8_t* sB = sm + 4 * 16384;              // 2 boxes [nb rows x 64 d_h]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + 2 * a.nb * 128);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
-  const int i = blockIdx.x;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+  const int i = blockIdx.x >> 1, half = blockIdx.x & 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bars[0], 1);  // weights landed
-    tc::mbar_init(&bars[1], 1);  // queries landed (one phase per N chunk)
-    tc::mbar_init(&bars[2], 1);  // MMAs done (one phase per N chunk)
+    tc::mbar_init(&bars[0], 1);  // weights of M tile 0 landed
+    tc::mbar_init(&bars[1], 1);  // weights of M tile 1 landed
+    tc::mbar_init(&bars[2], 1);  // queries landed (one phase per N chunk)
+    tc::mbar_init(&bars[3], 1);  // MMAs done (one phase per N chunk)
     tc::fence_mbar_init();
     tc::tma_prefetch_map(&map_wuk);
     tc::tma_prefetch_map(&map_qn);
+    for (int mt = 0; mt < 2; ++mt) {
+      tc::mbar_arrive_expect_tx(&bars[mt], 2 * 16384);
+      for (int j = 0; j < 2; ++j)
+        tc::tma_load_2d(sA + (2 * mt + j) * 16384, &map_wuk, 256 * half + 128 * mt + 64 * j, i * kDh, &bars[mt]);
+    }
   }
-  if (warp == 0) tc::tmem_alloc<512>(tslot);
+  if (warp == 0) tc::tmem_alloc<256>(tslot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tm = *tslot;
-  if (threadIdx.x == 0) {
-    tc::mbar_arrive_expect_tx(&bars[0], 8 * 16384);
-    for (int j = 0; j < 8; ++j) tc::tma_load_2d(sA + j * 16384, &map_wuk, 64 * j, i * kDh, &bars[0]);
-  }
-  // q_rope -> Q_lat chunks 64..71 of head i
-  for (int idx = threadIdx.x; idx < a.batch * 8; idx += kAbsorbThreads) {
-    const int b = idx >> 3, c = idx & 7;
-    const uint4 v = reinterpret_cast<const uint4*>(a.q_rope + (static_cast<int64_t>(b) * kH + i) * kDr)[c];
-    *reinterpret_cast<uint4*>(a.q_lat + qlat_index(b, kDc / 8 + c, i)) = v;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // q_rope -> Q_lat chunks 64..71 of head i (one of the two CTAs)
+  if (half == 0) {
+    for (int idx = threadIdx.x; idx < a.batch * 8; idx += kAbsorbThreads) {
+      const int b = idx >> 3, c = idx & 7;
+      const uint4 v = reinterpret_cast<const uint4*>(a.q_rope + (static_cast<int64_t>(b) * kH + i) * kDr)[c];
+      *reinterpret_cast<uint4*>(a.q_lat + qlat_index(b, kDc / 8 + c, i)) = v;
+    }
   }
   const uint32_t idesc = tc::idesc_bf16_f32(128, a.nb, 1, 0);
   bool ok = true;
   int chunk = 0;
   for (int n0 = 0; n0 < a.batch; n0 += a.nb, ++chunk) {
     if (threadIdx.x == 0) {
-      tc::mbar_arrive_expect_tx(&bars[1], 2 * a.nb * 128);
-      tc::tma_load_2d(sB, &map_qn, i * kDh, n0, &bars[1]);
-      tc::tma_load_2d(sB + a.nb * 128, &map_qn, i * kDh + 64, n0, &bars[1]);
-      ok = tc::mbar_wait(&bars[0], 0) && tc::mbar_wait(&bars[1], chunk & 1);
-      tc::tc_fence_after();
-      if (ok) {
-        for (int mt = 0; mt < 4; ++mt) {
+      tc::mbar_arrive_expect_tx(&bars[2], 2 * a.nb * 128);
+      tc::tma_load_2d(sB, &map_qn, i * kDh, n0, &bars[2]);
+      tc::tma_load_2d(sB + a.nb * 128, &map_qn, i * kDh + 64, n0, &bars[2]);
+      ok = tc::mbar_wait(&bars[2], chunk & 1);
+      for (int mt = 0; mt < 2 && ok; ++mt) {
+        ok = tc::mbar_wait(&bars[mt], 0);
+        tc::tc_fence_after();
+        if (ok) {
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + (2 * mt) * 16384 + 2048 * kk), 16384, 1024);
             const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sB + (kk >> 2) * a.nb * 128 + (kk & 3) * 32), 16, 1024);
-            tc::mma_ss(tm + mt * a.nb, ad, bd, idesc, kk > 0);
+            tc::mma_ss(tm + mt * a.nb, ad, bd, idesc, kk > 0 ? 1u : 0u);
           }
         }
       }
-      tc::mma_commit(&bars[2]);
+      tc::mma_commit(&bars[3]);
     }
     __syncwarp();
-    ok = tc::mbar_wait(&bars[2], chunk & 1);
+    ok = tc::mbar_wait(&bars[3], chunk & 1);
     tc::tc_fence_after();
     // epilogue: lane = latent row within the M tile, columns = sequences
-    for (int mt = 0; mt < 4; ++mt) {
+    for (int mt = 0; mt < 2; ++mt) {
       for (int c0 = 0; c0 < a.nb; c0 += 16) {
         uint32_t r[16];
         tc::tmem_ld16(tc::tmem_at(tm, 32 * warp, mt * a.nb + c0), r);
@@ -197,7 +236,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const int b = n0 + c0 + c;
-          const int k = mt * 128 + 32 * warp + lane;   // latent element
+          const int k = 256 * half + mt * 128 + 32 * warp + lane;   // latent element
           if (b < a.batch && ok)
             a.q_lat[qlat_index(b, k >> 3, i) + (k & 7)] = f32_to_bf16_bits(__uint_as_float(r[c]));
         }
@@ -206,7 +245,7 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
     tc::tc_fence_before();
     __syncthreads();  // TMEM and the query box are reused by the next chunk
   }
-  if (warp == 0) tc::tmem_dealloc<512>(tm);
+  if (warp == 0) tc::tmem_dealloc<256>(tm);
 }
 
 // ================================================================== attend
@@ -224,7 +263,7 @@ struct AttendArgs {
 struct AttendSmem {
   uint64_t full[kStages], empty[kStages];       // latent ring
   uint64_t rfull[kRopeStages], rempty[kRopeStages];  // rope ring (CTA0)
-  uint64_t s_full, s_free, p_full, o_done, q_ready, o_free, drain;
+  uint64_t s_full, s_free, p_full, o_done, q_ready, o_free, drain, drain2;
   uint64_t xfull[2];          // peer partial scores landed in xbuf[0/1] (byte-counted)
   uint64_t pair_max[4][2];    // the two softmax warps of a lane quarter swapped row maxima (by tile parity)
   uint64_t pair_sum[4];       // ... and row sums at a segment end
@@ -251,17 +290,13 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ SegIter seg_begin(const int32_t* cum, int batch, uint32_t c, uint32_t nc) {
-  const int64_t T = cum[batch];
+__device__ __forceinline__ SegIter seg_begin(const Plan& plan, int batch, uint32_t c, uint32_t nc) {
+  (void)batch;
+  (void)nc;
   SegIter it;
-  it.t = share_begin(c, T, nc);
-  it.t1 = share_begin(c + 1, T, nc);
-  int lo = 0, hi = batch;  // cum[lo] <= t < cum[hi] when t < T
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (cum[mid] <= it.t) lo = mid; else hi = mid;
-  }
-  it.b = lo;
+  it.t = plan.share_start[c];
+  it.t1 = plan.share_start[c + 1];
+  it.b = plan.first_seq[c];
   return it;
 }
 
@@ -369,6 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     tc::mbar_init(&S->q_ready, kSoftmaxThreads);
     tc::mbar_init(&S->o_free, kSoftmaxThreads);
     tc::mbar_init(&S->drain, 1);
+    tc::mbar_init(&S->drain2, 1);
     tc::mbar_init(&S->xfull[0], 1);
     tc::mbar_init(&S->xfull[1], 1);
     for (int q = 0; q < 4; ++q) {
@@ -396,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     // ---------------------------------------------------------------- TMA producer (whole warp walks
     // the tiles; lane l looks up the page of the l-th tile of each group of 32, lane 0 issues)
     const uint64_t policy = tc::policy_evict_first();
-    SegIter si = seg_begin(cum, a.batch, cl, ncl);
+    SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
     int b, j0, j1;
     uint32_t it = 0;
     bool ok = true;
@@ -456,58 +492,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    // Order: S(it), then PV(it-2): the scores of the next tile never wait for
-    // the softmax of the previous one. Every signal the softmax warps give
-    // while working on segment k comes after the epilogue of segment k-1,
-    // which needs all PVs of that segment: before waiting on such a signal,
-    // the PVs of all older segments are issued (flush_before).
+    // ---------------------------------------------------------------- score MMA issuer
+    // S(it) as soon as its tile has landed and the softmax has copied S(it-1)
+    // out of TMEM; the PVs go out from warp 2, so neither stream waits for the other.
     if (lane == 0) {
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, kTile, 0, 0);
-      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t desc0 = tc::sdesc_sw128(tc::smem_u32(tiles), 16, 1024);      // K-major tile, stage 0
       const uint64_t rdesc0 = tc::sdesc_sw128(tc::smem_u32(ropes), 16, 1024);     // K-major rope box, stage 0
-      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(tiles), kBlk, 1024);   // MN-major V, stage 0
-      SegIter si = seg_begin(cum, a.batch, cl, ncl);
+      SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
       int b, j0, j1;
       uint32_t it = 0, seg = 0;
       bool ok = true;
-      // tiles whose PV is still to be issued, oldest first
-      uint32_t pq_it[3] = {0, 0, 0}, pq_first[3] = {0, 0, 0}, pq_seg[3] = {0, 0, 0};
-      uint32_t pend_n = 0;
-      auto pv_oldest = [&]() -> bool {
-        const uint32_t q = pq_it[0], first = pq_first[0], sg = pq_seg[0];
-        if (!tc::mbar_wait(&S->p_full, q & 1)) return false;
-        if (first && sg > 0 && !tc::mbar_wait(&S->o_free, (sg - 1) & 1)) return false;
-        tc::tc_fence_after();
-        const uint32_t st = q % kStages;
-        issue_pv(tm + kTmO, tm + kTmP, vdesc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_o,
-                 first ? 0u : 1u);
-        tc::mma_commit(&S->o_done);
-        tc::mma_commit(&S->empty[st]);
-        pq_it[0] = pq_it[1]; pq_first[0] = pq_first[1]; pq_seg[0] = pq_seg[1];
-        pq_it[1] = pq_it[2]; pq_first[1] = pq_first[2]; pq_seg[1] = pq_seg[2];
-        --pend_n;
-        return true;
-      };
-      auto flush_before = [&](uint32_t sg) -> bool {   // issue pending PVs of segments < sg
-        bool good = true;
-        while (good && pend_n > 0 && pq_seg[0] < sg) good = pv_oldest();
-        return good;
-      };
-      uint32_t prev_seg = 0;   // segment of tile it-1
       while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
-        // q_ready of segment `seg` comes from the last tile of segment seg-1
-        if (seg >= 2) ok = flush_before(seg - 1);
-        if (ok) ok = tc::mbar_wait(&S->q_ready, seg & 1);
+        ok = tc::mbar_wait(&S->q_ready, seg & 1);
         for (int j = j0; j < j1 && ok; ++j, ++it) {
           const uint32_t st = it % kStages, rs = it % kRopeStages;
           ok = tc::mbar_wait(&S->full[st], (it / kStages) & 1);
           if (ok && rank == 0) ok = tc::mbar_wait(&S->rfull[rs], (it / kRopeStages) & 1);
-          if (ok && it > 0) {
-            ok = flush_before(prev_seg);   // s_free(it-1) comes from tile it-1's segment
-            if (ok) ok = tc::mbar_wait(&S->s_free, (it - 1) & 1);
-          }
+          if (ok && it > 0) ok = tc::mbar_wait(&S->s_free, (it - 1) & 1);
           if (!ok || aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
           issue_scores<16>(tm + kTmS, tm + kTmQ, desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_s, 1u);
@@ -516,20 +518,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
             tc::mma_commit(&S->rempty[rs]);
           }
           tc::mma_commit(&S->s_full);
-          pq_it[pend_n] = it;
-          pq_first[pend_n] = (j == j0) ? 1u : 0u;
-          pq_seg[pend_n] = seg;
-          ++pend_n;
-          prev_seg = seg;
-          if (pend_n == 3) ok = pv_oldest();
         }
         ++seg;
       }
-      while (ok && pend_n > 0) ok = pv_oldest();
       if (!ok) set_abort(S);
       // every MMA issued so far must complete before TMEM is released
       tc::mma_commit(&S->drain);
       tc::mbar_wait(&S->drain, 0);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- PV MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(tiles), kBlk, 1024);   // MN-major V, stage 0
+      SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
+      int b, j0, j1;
+      uint32_t it = 0, seg = 0;
+      bool ok = true;
+      while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+        for (int j = j0; j < j1 && ok; ++j, ++it) {
+          // P(it) in TMEM implies S(it), hence its tile, were complete
+          ok = tc::mbar_wait(&S->p_full, it & 1);
+          if (ok && j == j0 && seg > 0) ok = tc::mbar_wait(&S->o_free, (seg - 1) & 1);
+          if (!ok || aborted(S)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t st = it % kStages;
+          issue_pv(tm + kTmO, tm + kTmP, vdesc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_o,
+                   j == j0 ? 0u : 1u);
+          tc::mma_commit(&S->o_done);
+          tc::mma_commit(&S->empty[st]);
+        }
+        ++seg;
+      }
+      if (!ok) set_abort(S);
+      tc::mma_commit(&S->drain2);
+      tc::mbar_wait(&S->drain2, 0);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
@@ -554,7 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     const uint32_t peer_bar1 = tc::map_peer(&S->xfull[1], peer);
     const float sl = a.scale_log2;
 
-    SegIter si = seg_begin(cum, a.batch, cl, ncl);
+    SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
     int b, j0, j1;
     uint32_t it = 0;
     bool ok = true;
@@ -578,15 +601,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       {
         const uint8_t* xr = xbuf + xb * kXbufBytes;
         const float pun = reinterpret_cast<const float*>(xr + kXvalBytes)[half * kH + h];
+        uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xr + xoff(u));
-          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(xr + xoff(u));
+        if (pun == 1.f && pend_un == 1.f) {   // the usual case: no rescaling of either half
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t ow = pend[4 * u + e];
-            s[8 * u + 2 * e] = f16_lo(ow) * pend_un + f16_lo(pw[e]) * pun;
-            s[8 * u + 2 * e + 1] = f16_hi(ow) * pend_un + f16_hi(pw[e]) * pun;
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t pw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t ow = pend[4 * u + e];
+              s[8 * u + 2 * e] = f16_lo(ow) + f16_lo(pw[e]);
+              s[8 * u + 2 * e + 1] = f16_hi(ow) + f16_hi(pw[e]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t pw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t ow = pend[4 * u + e];
+              s[8 * u + 2 * e] = f16_lo(ow) * pend_un + f16_lo(pw[e]) * pun;
+              s[8 * u + 2 * e + 1] = f16_hi(ow) * pend_un + f16_hi(pw[e]) * pun;
+            }
           }
         }
       }
@@ -595,9 +633,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) if (c >= vh) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      float mx;
+      {
+        float t8[8];
 #pragma unroll
-      for (int c = 1; c < 32; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < 8; ++c) t8[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
+        mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+      }
       S->red[q & 1][half][h] = mx;
       tc::mbar_arrive(&S->pair_max[quarter][q & 1]);
       if (!tc::mbar_wait(&S->pair_max[quarter][q & 1], (q >> 1) & 1)) return false;
@@ -614,13 +656,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       }
       const float neg_m = -m_used;
       uint32_t p[16];
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
         const uint32_t w = tc::pack_bf16(tc::ex2_approx(fmaf(s[c], sl, neg_m)), tc::ex2_approx(fmaf(s[c + 1], sl, neg_m)));
         p[c / 2] = w;
-        psum += bf_lo(w) + bf_hi(w);
+        ps[(c / 2) & 3] += bf_lo(w) + bf_hi(w);
       }
+      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
       l += psum;
       // PV of the previous tile must be done: the P buffer and O are ours
       if (q > 0 && !tc::mbar_wait(&S->o_done, (q - 1) & 1)) return false;
@@ -635,7 +678,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
           tc::tmem_st16(t_o + c0, r);
         }
       }
-      tc::tmem_st16(t_p, p);
+      tc::tmem_st16(t_p, p);   // completed by finish_commit, after this tile's send
+      return true;
+    };
+
+    // Completes tile `q`: its P store, the rows past the sequence end, the hand-off to the PV warp.
+    auto finish_commit = [&](uint32_t q, int valid) {
       tc::tmem_st_wait();
       // rows past the sequence end must not reach PV as NaN/Inf garbage
       if (valid < kTile) {
@@ -650,7 +698,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&S->p_full);
-      return true;
     };
 
     while (ok && have) {
@@ -683,15 +730,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
               if (16 + c >= vh) r1[c] = 0u;
             }
           }
-          float amax = 0.f;
+          float am[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(r0[c])), fabsf(__uint_as_float(r1[c]))));
+          for (int c = 0; c < 8; ++c)
+            am[c] = fmaxf(fmaxf(fabsf(__uint_as_float(r0[2 * c])), fabsf(__uint_as_float(r0[2 * c + 1]))),
+                          fmaxf(fabsf(__uint_as_float(r1[2 * c])), fabsf(__uint_as_float(r1[2 * c + 1]))));
+          const float amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])),
+                                   fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
           const float sc = exchange_scale(amax, &own_un);
+          if (sc != 1.f) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              r0[c] = __float_as_uint(__uint_as_float(r0[c]) * sc);
+              r1[c] = __float_as_uint(__uint_as_float(r1[c]) * sc);
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            own[c] = pack_f16(__uint_as_float(r0[2 * c]) * sc, __uint_as_float(r0[2 * c + 1]) * sc);
-            own[8 + c] = pack_f16(__uint_as_float(r1[2 * c]) * sc, __uint_as_float(r1[2 * c + 1]) * sc);
+            own[c] = pack_f16(__uint_as_float(r0[2 * c]), __uint_as_float(r0[2 * c + 1]));
+            own[8 + c] = pack_f16(__uint_as_float(r1[2 * c]), __uint_as_float(r1[2 * c + 1]));
           }
         }
         tc::tc_fence_before();
@@ -713,6 +770,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
             tc::st_async_v4(dst + xoff(u), bar, own[4 * u], own[4 * u + 1], own[4 * u + 2], own[4 * u + 3]);
           tc::st_async_b32(dst + kXvalBytes + 4 * (half * kH + h), bar, __float_as_uint(own_un));
         }
+        if (have_pend) finish_commit(pend_it, pend_valid);
         if (j == j1 - 1 && have_next) load_q(nb_);   // all score MMAs of this segment are done
 #pragma unroll
         for (int c = 0; c < 16; ++c) pend[c] = own[c];
@@ -725,6 +783,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       ok = finish(pend_it, pend_valid);
       have_pend = false;
       if (!ok) break;
+      finish_commit(pend_it, pend_valid);
       // ---- segment epilogue: unnormalised O half, m and l
       ok = tc::mbar_wait(&S->o_done, (it - 1) & 1);
       if (!ok) break;
@@ -787,7 +846,7 @@ struct MergeArgs {
   int batch, ncl;
 };
 
-constexpr int kMergeChunks = 4;                  // 4-float chunks per CTA (16 latent elements)
+constexpr int kMergeChunks = 1;                  // 4-float chunks per CTA (4 latent elements)
 constexpr int kMergeSplit = kOChunks / kMergeChunks;   // CTAs per sequence
 
 // One CTA per (sequence b, 16 latent elements); thread = head. o_lat =
@@ -800,19 +859,18 @@ __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
   const int h = threadIdx.x;
   const int b = blockIdx.y;
   const int chunk0 = blockIdx.x * kMergeChunks;
-  const int64_t T = a.plan.cum[a.batch];
-  const int64_t tb0 = a.plan.cum[b], tb1 = a.plan.cum[b + 1];
+  const int c0 = a.plan.seq_c0[b], c1 = a.plan.seq_c1[b];   // c1 < c0: no tiles, output 0
+  const int32_t* start = a.plan.share_start;
   float4 acc[kMergeChunks];
 #pragma unroll
   for (int k = 0; k < kMergeChunks; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (T > 0 && tb1 > tb0) {
-    const int64_t c0 = share_owner(tb0, T, a.ncl), c1 = share_owner(tb1 - 1, T, a.ncl);
+  if (c1 >= c0) {
     const float2* ml_all = reinterpret_cast<const float2*>(a.part_ml);
     // running max and denominator in one pass
     float M = -INFINITY, den = 0.f;
-    for (int64_t c = c0; c <= c1; ++c) {
-      if (share_begin(c, T, a.ncl) == share_begin(c + 1, T, a.ncl)) continue;   // empty share: no partial
-      const float2 ml = ml_all[(b + c) * kH + h];
+    for (int c = c0; c <= c1; ++c) {
+      if (start[c] == start[c + 1]) continue;   // empty share: no partial
+      const float2 ml = ml_all[static_cast<int64_t>(b + c) * kH + h];
       if (ml.x > M) {
         den = den * exp2f(M - ml.x) + ml.y;
         M = ml.x;
@@ -822,9 +880,9 @@ __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll 2
-    for (int64_t c = c0; c <= c1; ++c) {
-      if (share_begin(c, T, a.ncl) == share_begin(c + 1, T, a.ncl)) continue;
-      const float w = exp2f(ml_all[(b + c) * kH + h].x - M) * inv;
+    for (int c = c0; c <= c1; ++c) {
+      if (start[c] == start[c + 1]) continue;
+      const float w = exp2f(ml_all[static_cast<int64_t>(b + c) * kH + h].x - M) * inv;
       float4 v[kMergeChunks];
 #pragma unroll
       for (int k = 0; k < kMergeChunks; ++k)
@@ -840,17 +898,17 @@ __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
   }
   const int64_t row = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * chunk0;
 #pragma unroll
-  for (int k = 0; k < kMergeChunks; k += 2) {
-    const float v[8] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w, acc[k + 1].x, acc[k + 1].y, acc[k + 1].z, acc[k + 1].w};
-    uint32_t hi[4], lo[4];
+  for (int k = 0; k < kMergeChunks; ++k) {
+    const float v[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+    uint32_t hi[2], lo[2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 2; ++u) {
       hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
       lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
                             v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
     }
-    *reinterpret_cast<uint4*>(a.o_hi + row + 4 * k) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(a.o_lo + row + 4 * k) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint2*>(a.o_hi + row + 4 * k) = make_uint2(hi[0], hi[1]);
+    *reinterpret_cast<uint2*>(a.o_lo + row + 4 * k) = make_uint2(lo[0], lo[1]);
   }
 }
 

@@ -172,7 +172,7 @@ constexpr int kMaxClusters = 128;
 
 struct TcPlan {
   int nb, slots;
-  size_t off_qlat, off_lens, off_cum, off_ml, off_o, off_hi, off_lo, bytes;
+  size_t off_qlat, off_lens, off_cum, off_first, off_start, off_c0, off_c1, off_ml, off_o, off_hi, off_lo, bytes;
 };
 
 TcPlan tc_plan(int batch) {
@@ -186,6 +186,14 @@ TcPlan tc_plan(int batch) {
   off = align_up(off + static_cast<size_t>(batch) * 4, 256);
   p.off_cum = off;
   off = align_up(off + static_cast<size_t>(batch + 1) * 4, 256);
+  p.off_first = off;
+  off = align_up(off + static_cast<size_t>(kMaxClusters) * 4, 256);
+  p.off_start = off;
+  off = align_up(off + static_cast<size_t>(kMaxClusters + 1) * 4, 256);
+  p.off_c0 = off;
+  off = align_up(off + static_cast<size_t>(batch) * 4, 256);
+  p.off_c1 = off;
+  off = align_up(off + static_cast<size_t>(batch) * 4, 256);
   p.off_ml = off;
   off = align_up(off + static_cast<size_t>(p.slots) * tcd::kH * 8, 256);
   p.off_o = off;
@@ -202,7 +210,7 @@ constexpr size_t kAttendSmem = 1024 + tcd::kStages * tcd::kStageBytes + tcd::kRo
                                2 * tcd::kXbufBytes + sizeof(tcd::AttendSmem);
 static_assert(kAttendSmem <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
 constexpr size_t kUvSmem = 1024 + tcd::kUvSmem;
-size_t absorb_smem(int nb) { return 1024 + 8 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
+size_t absorb_smem(int nb) { return 1024 + 4 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
 
 struct TcDeviceState {
   bool ready = false;
@@ -277,7 +285,9 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   mla_status s = tc_device_setup(&ncl);
   if (s != MLA_OK) return s;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  tcd::Plan plan{reinterpret_cast<int32_t*>(ws + p.off_lens), reinterpret_cast<int32_t*>(ws + p.off_cum)};
+  tcd::Plan plan{reinterpret_cast<int32_t*>(ws + p.off_lens), reinterpret_cast<int32_t*>(ws + p.off_cum),
+                 reinterpret_cast<int32_t*>(ws + p.off_first), reinterpret_cast<int32_t*>(ws + p.off_start),
+                 reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
   CUtensorMap m_pool, m_wuk, m_wuv, m_qn, m_hi, m_lo;
@@ -304,6 +314,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   aa.batch = batch;
   aa.nb = p.nb;
   aa.max_seq_len = max_seq_len;
+  aa.ncl = ncl;
 
   tcd::AttendArgs ta{};
   ta.q_lat = q_lat;
@@ -331,9 +342,10 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   ua.batch = batch;
 
   stage_mark(0, st);
-  tcd::absorb_tc_kernel<<<tcd::kH + 1, tcd::kAbsorbThreads, absorb_smem(p.nb), st>>>(m_wuk, m_qn, aa);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "absorb launch");
+  void* absorb_args[] = {&m_wuk, &m_qn, &aa};
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::absorb_tc_kernel), dim3(2 * tcd::kH + 1), dim3(tcd::kAbsorbThreads),
+                 absorb_smem(p.nb), st, absorb_args);
+  if (s != MLA_OK) return s;
   stage_mark(1, st);
   void* attend_args[] = {&m_pool, &ta};
   s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_tc_kernel), dim3(2 * ncl), dim3(tcd::kAttendThreads),
