@@ -34,13 +34,29 @@ constexpr int kH = 128, kDc = 512, kDr = 64, kDh = 128, kRow = 576;
 constexpr int kTile = 64;                    // tokens per attend tile
 constexpr int kBlk = kTile * 128;            // one TMA box: 64 rows x 64 bf16 (128 B) = 8 KB
 constexpr int kStageBytes = 4 * kBlk;        // latent boxes of one tile for one CTA: 256 columns
-constexpr int kStages = 5;                   // latent ring depth
+constexpr int kStages = 4;                   // latent ring depth (bf16 cache)
+constexpr int kStagesF8 = 3;                 // latent ring depth (FP8 cache: bf16 tiles dequantised in place)
 constexpr int kRopeStages = 3;               // rope ring depth (CTA0 only)
+constexpr int kRawStages = 3;                // FP8 cache: ring of raw rows (codes + block scales)
+constexpr int kRawCodeBytes = kTile * 256;   // this CTA's 256 E4M3 codes of 64 rows
+constexpr int kRawBytes = kRawCodeBytes + kTile * 16;   // + the 4 fp32 block scales of each row
+constexpr int kParts = 4;                    // softmax warps per TMEM lane quarter
+constexpr int kCols = kTile / kParts;        // score columns per softmax thread
 constexpr int kXvalBytes = kH * kTile * 2;   // one partial score tile as fp16
-constexpr int kXbufBytes = kXvalBytes + 2 * kH * 4;   // + one power-of-two scale per (row, column half)
-constexpr int kSoftmaxThreads = 256;         // 8 warps: 4 TMEM lane quarters x 2 column halves
+constexpr int kXbufBytes = kXvalBytes + kParts * kH * 4;   // + one power-of-two scale per (row, column part)
+constexpr int kSoftmaxThreads = 128 * kParts;   // 4 TMEM lane quarters x kParts column parts
 constexpr int kAttendThreads = 128 + kSoftmaxThreads;  // warp 0 TMA, warps 1-2 MMA, warps 4-11 softmax
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: O is rescaled only when the max grows by > 2^8
+
+// Shared-memory carve-up of the attend kernel (after 1 KB alignment), per cache format.
+template <bool kF8>
+struct AttendLayout {
+  static constexpr int kSt = kF8 ? kStagesF8 : kStages;
+  static constexpr int kRaw = kF8 ? kRawStages : 0;
+  static constexpr size_t kRopes = static_cast<size_t>(kSt) * kStageBytes;
+  static constexpr size_t kRawOff = kRopes + static_cast<size_t>(kRopeStages) * kBlk;
+  static constexpr size_t kXbuf = kRawOff + static_cast<size_t>(kRaw) * kRawBytes;
+};
 
 // TMEM columns of the attend kernel (512 allocated)
 constexpr uint32_t kTmO = 0;     // O half: 128 lanes x 256 fp32
@@ -257,18 +273,20 @@ struct AttendArgs {
   float* part_ml;             // [slots, H, 2]: running max (log2 units) and sum
   int64_t num_pages;
   int batch, max_pages, page_size;
+  int rope_x;                 // column of the rope box in the rope tensor map
   float scale_log2;           // softmax scale * log2(e), > 0
 };
 
 struct AttendSmem {
-  uint64_t full[kStages], empty[kStages];       // latent ring
+  uint64_t full[kStages], empty[kStages];       // latent ring (bf16 tiles, however they were filled)
+  uint64_t raw_full[kRawStages], raw_empty[kRawStages];   // FP8 cache: raw rows
   uint64_t rfull[kRopeStages], rempty[kRopeStages];  // rope ring (CTA0)
   uint64_t s_full, s_free, p_full, o_done, q_ready, o_free, drain, drain2;
   uint64_t xfull[2];          // peer partial scores landed in xbuf[0/1] (byte-counted)
-  uint64_t pair_max[4][2];    // the two softmax warps of a lane quarter swapped row maxima (by tile parity)
+  uint64_t pair_max[4][2];    // the softmax warps of a lane quarter swapped row maxima (by tile parity)
   uint64_t pair_sum[4];       // ... and row sums at a segment end
-  float red[2][2][kH];        // per-half row maxima, by tile parity, shared by the two softmax halves
-  float redl[2][kH];          // per-half row sums at a segment end
+  float red[2][kParts][kH];   // per-part row maxima, by tile parity
+  float redl[kParts][kH];     // per-part row sums at a segment end
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -326,29 +344,39 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t b0, ui
   for (int k = 1; k < 4; ++k) tc::mma_ts(d, a + 8 * k, b0 + static_cast<uint64_t>((k * 2048) >> 4), idesc, 1u);
 }
 
-// This half's share of the Q slice of sequence b (row h) into TMEM columns
+// This part's share of the Q slice of sequence b (row h) into TMEM columns
 // kTmQ.. as bf16 pairs. CTA0's slice is latent 0..255 then rope 512..575
-// (40 chunks of 16 bytes), CTA1's latent 256..511 (32 chunks); half 0 takes
-// the first half of the chunks.
+// (40 chunks of 16 bytes), CTA1's latent 256..511 (32 chunks); part p takes
+// chunks p * NCH/kParts .. (p+1) * NCH/kParts - 1.
 template <int NCH>
-__device__ __forceinline__ void load_q_half(const uint16_t* q_lat, int b, int h, uint32_t rank, int half,
+__device__ __forceinline__ void load_q_part(const uint16_t* q_lat, int b, int h, uint32_t rank, int part,
                                             uint32_t taddr) {
-  constexpr int kHalf = NCH / 2;
-  uint4 v[kHalf];
+  constexpr int kPer = NCH / kParts;
+  uint4 v[kPer];
 #pragma unroll
-  for (int u = 0; u < kHalf; ++u) {
-    const int c = half * kHalf + u;   // chunk of this CTA's slice
+  for (int u = 0; u < kPer; ++u) {
+    const int c = part * kPer + u;   // chunk of this CTA's slice
     const int qc = rank == 0 ? (c < 32 ? c : kDc / 8 + (c - 32)) : 32 + c;
     v[u] = *reinterpret_cast<const uint4*>(q_lat + qlat_index(b, qc, h));
   }
+  const uint32_t t0 = taddr + 4 * part * kPer;
 #pragma unroll
-  for (int u = 0; u < kHalf; u += 4) {
+  for (int u = 0; u + 4 <= kPer; u += 4) {
     uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       w[4 * e] = v[u + e].x; w[4 * e + 1] = v[u + e].y; w[4 * e + 2] = v[u + e].z; w[4 * e + 3] = v[u + e].w;
     }
-    tc::tmem_st16(taddr + 4 * (half * kHalf + u), w);
+    tc::tmem_st16(t0 + 4 * u, w);
+  }
+  if constexpr (kPer % 4 == 2) {
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      w[4 * e] = v[kPer - 2 + e].x; w[4 * e + 1] = v[kPer - 2 + e].y;
+      w[4 * e + 2] = v[kPer - 2 + e].z; w[4 * e + 3] = v[kPer - 2 + e].w;
+    }
+    tc::tmem_st8(t0 + 4 * (kPer - 2), w);
   }
   tc::tmem_st_wait();
 }
@@ -364,6 +392,23 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ float f16_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu))); }
 __device__ __forceinline__ float f16_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))); }
 
+// (f32)a.lo + (f32)b.lo and (f32)a.hi + (f32)b.hi for two fp16 pairs, on the
+// fp32 pipe (mixed-precision adds convert their fp16 operand exactly); equal
+// to converting both and adding, and symmetric in a and b.
+__device__ __forceinline__ float2 add_f16x2_f32(uint32_t a, uint32_t b) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 t0, t1;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {bl, bh}, %3;\n\t"
+      "add.rn.f32.f16 t0, bl, 0f00000000;\n\t"
+      "add.rn.f32.f16 %0, al, t0;\n\t"
+      "add.rn.f32.f16 t1, bh, 0f00000000;\n\t"
+      "add.rn.f32.f16 %1, ah, t1;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(a), "r"(b));
+  return make_float2(lo, hi);
+}
+
 // Partial scores travel between the two CTAs as fp16 scaled by 2^-k, with k
 // chosen per (row, column half) so that the largest magnitude stays below
 // 2^15: no overflow whatever the inputs, 11 significant bits. Both CTAs add
@@ -375,13 +420,25 @@ __device__ __forceinline__ float exchange_scale(float amax, float* unscale) {
   return __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
 }
 
+// kF8 = false: map_lat is the bf16 pool [rows, 576], boxes of 64 x 64 (128-byte swizzle);
+//              map_scale is unused.
+// kF8 = true:  map_lat and map_scale are byte views of the FP8 pool [rows, 656] with unswizzled
+//              boxes of 64 rows x 256 codes (this CTA's half, column 256 * rank) and of
+//              64 rows x 16 bytes (the four block scales, column 512); the softmax threads
+//              dequantise them into the same bf16 tile layout the TMA gives a bf16 pool.
+// map_rope: the 64 rope values of each row as bf16, box 64 x 64 at column a.rope_x.
+template <bool kF8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
-    attend_tc_kernel(const __grid_constant__ CUtensorMap map_pool, AttendArgs a) {
+    attend_tc_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_scale,
+                     const __grid_constant__ CUtensorMap map_rope, AttendArgs a) {
+  using LY = AttendLayout<kF8>;
+  constexpr int kSt = LY::kSt;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* tiles = sm;                                           // kStages x 32 KB latent boxes
-  uint8_t* ropes = sm + kStages * kStageBytes;                   // kRopeStages x 8 KB (CTA0)
-  uint8_t* xbuf = ropes + kRopeStages * kBlk;                    // 2 x [128 heads x 64] bf16
+  uint8_t* tiles = sm;                                           // kSt x 32 KB latent boxes (bf16)
+  uint8_t* ropes = sm + LY::kRopes;                              // kRopeStages x 8 KB (CTA0)
+  uint8_t* rawb = sm + LY::kRawOff;                              // FP8: kRawStages x raw rows
+  uint8_t* xbuf = sm + LY::kXbuf;                                // 2 x [128 heads x 64] partial scores
   AttendSmem* S = reinterpret_cast<AttendSmem*>(xbuf + 2 * kXbufBytes);
 
   const uint32_t rank = tc::cluster_ctarank(), peer = rank ^ 1u;
@@ -389,9 +446,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&S->full[s], 1);
+    for (int s = 0; s < kSt; ++s) {
+      tc::mbar_init(&S->full[s], kF8 ? kSoftmaxThreads : 1);   // FP8: every dequantising thread arrives
       tc::mbar_init(&S->empty[s], 1);
+    }
+    for (int s = 0; s < kRawStages; ++s) {
+      tc::mbar_init(&S->raw_full[s], 1);
+      tc::mbar_init(&S->raw_empty[s], kSoftmaxThreads);
     }
     for (int s = 0; s < kRopeStages; ++s) {
       tc::mbar_init(&S->rfull[s], 1);
@@ -408,16 +469,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     tc::mbar_init(&S->xfull[0], 1);
     tc::mbar_init(&S->xfull[1], 1);
     for (int q = 0; q < 4; ++q) {
-      tc::mbar_init(&S->pair_max[q][0], 64);
-      tc::mbar_init(&S->pair_max[q][1], 64);
-      tc::mbar_init(&S->pair_sum[q], 64);
+      tc::mbar_init(&S->pair_max[q][0], 32 * kParts);
+      tc::mbar_init(&S->pair_max[q][1], 32 * kParts);
+      tc::mbar_init(&S->pair_sum[q], 32 * kParts);
     }
     S->abort_flag = 0;
     tc::fence_mbar_init();
     // both exchange buffers expect one partial score tile from the peer
     tc::mbar_arrive_expect_tx(&S->xfull[0], kXbufBytes);
     tc::mbar_arrive_expect_tx(&S->xfull[1], kXbufBytes);
-    tc::tma_prefetch_map(&map_pool);
+    tc::tma_prefetch_map(&map_lat);
+    if (kF8) tc::tma_prefetch_map(&map_scale);
+    tc::tma_prefetch_map(&map_rope);
   }
   if (warp == 1) tc::tmem_alloc<512>(&S->tmem_base);
   tc::tc_fence_before();
@@ -458,19 +521,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
         for (int u = 0; u < n; ++u) {
           const int32_t y = __shfl_sync(0xffffffffu, y_l, u);
           if (lane == 0 && ok) {
-            const int st = it % kStages, rs = it % kRopeStages;
-            if (it >= kStages) ok = tc::mbar_wait(&S->empty[st], ((it / kStages) - 1) & 1);
+            const int st = it % kSt, rs = it % kRopeStages, ws = it % kRawStages;
+            if (kF8) {
+              if (it >= kRawStages) ok = tc::mbar_wait(&S->raw_empty[ws], ((it / kRawStages) - 1) & 1);
+            } else {
+              if (it >= kSt) ok = tc::mbar_wait(&S->empty[st], ((it / kSt) - 1) & 1);
+            }
             if (ok && rank == 0 && it >= kRopeStages) ok = tc::mbar_wait(&S->rempty[rs], ((it / kRopeStages) - 1) & 1);
             if (ok && aborted(S)) ok = false;
             if (ok) {
-              uint8_t* dst = tiles + st * kStageBytes;
-              tc::mbar_arrive_expect_tx(&S->full[st], kStageBytes);
-              for (int k = 0; k < 4; ++k)
-                tc::tma_load_2d_hint(dst + k * kBlk, &map_pool, static_cast<int>(rank) * 256 + 64 * k, y,
-                                     &S->full[st], policy);
+              if (kF8) {
+                uint8_t* dst = rawb + ws * kRawBytes;
+                tc::mbar_arrive_expect_tx(&S->raw_full[ws], kRawBytes);
+                tc::tma_load_2d_hint(dst, &map_lat, static_cast<int>(rank) * 256, y, &S->raw_full[ws], policy);
+                tc::tma_load_2d_hint(dst + kRawCodeBytes, &map_scale, kDc, y, &S->raw_full[ws], policy);
+              } else {
+                uint8_t* dst = tiles + st * kStageBytes;
+                tc::mbar_arrive_expect_tx(&S->full[st], kStageBytes);
+                for (int k = 0; k < 4; ++k)
+                  tc::tma_load_2d_hint(dst + k * kBlk, &map_lat, static_cast<int>(rank) * 256 + 64 * k, y,
+                                       &S->full[st], policy);
+              }
               if (rank == 0) {
                 tc::mbar_arrive_expect_tx(&S->rfull[rs], kBlk);
-                tc::tma_load_2d_hint(ropes + rs * kBlk, &map_pool, kDc, y, &S->rfull[rs], policy);
+                tc::tma_load_2d_hint(ropes + rs * kBlk, &map_rope, a.rope_x, y, &S->rfull[rs], policy);
               }
               ++it;
             }
@@ -484,8 +558,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     if (lane == 0) {
       if (!ok) set_abort(S);
       // drain: copies still in flight must land before the CTA exits
-      const uint32_t first = it > kStages ? it - kStages : 0;
-      for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kStages], (q / kStages) & 1);
+      if (kF8) {
+        const uint32_t first = it > kRawStages ? it - kRawStages : 0;
+        for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->raw_full[q % kRawStages], (q / kRawStages) & 1);
+      } else {
+        const uint32_t first = it > kSt ? it - kSt : 0;
+        for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kSt], (q / kSt) & 1);
+      }
       if (rank == 0) {
         const uint32_t rfirst = it > kRopeStages ? it - kRopeStages : 0;
         for (uint32_t q = rfirst; q < it; ++q) tc::mbar_wait(&S->rfull[q % kRopeStages], (q / kRopeStages) & 1);
@@ -506,8 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
         ok = tc::mbar_wait(&S->q_ready, seg & 1);
         for (int j = j0; j < j1 && ok; ++j, ++it) {
-          const uint32_t st = it % kStages, rs = it % kRopeStages;
-          ok = tc::mbar_wait(&S->full[st], (it / kStages) & 1);
+          const uint32_t st = it % kSt, rs = it % kRopeStages;
+          ok = tc::mbar_wait(&S->full[st], (it / kSt) & 1);
           if (ok && rank == 0) ok = tc::mbar_wait(&S->rfull[rs], (it / kRopeStages) & 1);
           if (ok && it > 0) ok = tc::mbar_wait(&S->s_free, (it - 1) & 1);
           if (!ok || aborted(S)) { ok = false; break; }
@@ -542,7 +621,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
           if (ok && j == j0 && seg > 0) ok = tc::mbar_wait(&S->o_free, (seg - 1) & 1);
           if (!ok || aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
-          const uint32_t st = it % kStages;
+          const uint32_t st = it % kSt;
           issue_pv(tm + kTmO, tm + kTmP, vdesc0 + static_cast<uint64_t>((st * kStageBytes) >> 4), idesc_o,
                    j == j0 ? 0u : 1u);
           tc::mma_commit(&S->o_done);
@@ -556,22 +635,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax + epilogue
-    // 8 warps: warp w holds head rows 32 (w % 4) .. +31 (its TMEM lane quarter)
-    // and token columns 32 * half .. +31 of every tile.
-    const int quarter = warp & 3, half = (warp - 4) >> 2;
+    // kParts warps per TMEM lane quarter: warp w holds head rows 32 (w % 4) .. +31
+    // and token columns kCols * part .. + kCols - 1 of every tile.
+    const int quarter = warp & 3, part = (warp - 4) >> 2;
     const int h = 32 * quarter + lane;           // head = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    const uint32_t t_s = tm + lane_base + kTmS + 32 * half;
-    const uint32_t t_o = tm + lane_base + kTmO + 128 * half;
-    const uint32_t t_p = tm + lane_base + kTmP + 16 * half;
+    const uint32_t t_s = tm + lane_base + kTmS + kCols * part;
+    const uint32_t t_o = tm + lane_base + kTmO + (256 / kParts) * part;
+    const uint32_t t_p = tm + lane_base + kTmP + (kCols / 2) * part;
     auto load_q = [&](int bq) {
-      if (rank == 0) load_q_half<40>(a.q_lat, bq, h, rank, half, tm + lane_base + kTmQ);
-      else load_q_half<32>(a.q_lat, bq, h, rank, half, tm + lane_base + kTmQ);
+      if (rank == 0) load_q_part<40>(a.q_lat, bq, h, rank, part, tm + lane_base + kTmQ);
+      else load_q_part<32>(a.q_lat, bq, h, rank, part, tm + lane_base + kTmQ);
       tc::tc_fence_before();
       tc::mbar_arrive(&S->q_ready);
     };
-    // this thread's 64 bytes of row h in the exchange buffers (16-byte chunks 4*half .. +3, swizzled)
-    auto xoff = [&](int q) { return h * 128 + (((4 * half + q) ^ (h & 7)) << 4); };
+    // this thread's 32 bytes of row h in the exchange buffers (16-byte chunks 2 part, 2 part + 1, swizzled)
+    auto xoff = [&](int u) { return h * 128 + (((2 * part + u) ^ (h & 7)) << 4); };
     const uint32_t peer_x = tc::map_peer(xbuf, peer);
     const uint32_t peer_bar0 = tc::map_peer(&S->xfull[0], peer);
     const uint32_t peer_bar1 = tc::map_peer(&S->xfull[1], peer);
@@ -583,8 +662,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     bool ok = true;
     bool have = si.next(cum, a.batch, &b, &j0, &j1);
     if (have) load_q(b);
-    // the tile waiting for its peer half: its own partial scores as bf16 pairs
-    uint32_t pend[16];
+    // the tile waiting for its peer half: this thread's own partial scores (scaled fp16 pairs)
+    uint32_t pend[kCols / 2];
     float pend_un = 1.f;
     bool have_pend = false;
     int pend_valid = 0;
@@ -592,58 +671,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     uint32_t n_epi = 0;   // segment epilogues done (phase of pair_sum)
 
-    // Finishes tile `q`: full scores, online softmax, P to TMEM.
+    // Finishes tile `q` up to its P store: full scores, online softmax.
     auto finish = [&](uint32_t q, int valid) -> bool {
       const uint32_t xb = q & 1u;
       if (!tc::mbar_wait(&S->xfull[xb], (q >> 1) & 1)) return false;
-      if (h == 0 && half == 0) tc::mbar_arrive_expect_tx(&S->xfull[xb], kXbufBytes);   // arm its next use
-      float s[32];
+      if (h == 0 && part == 0) tc::mbar_arrive_expect_tx(&S->xfull[xb], kXbufBytes);   // arm its next use
+      float s[kCols];
       {
         const uint8_t* xr = xbuf + xb * kXbufBytes;
-        const float pun = reinterpret_cast<const float*>(xr + kXvalBytes)[half * kH + h];
-        uint4 v[4];
+        const float pun = reinterpret_cast<const float*>(xr + kXvalBytes)[part * kH + h];
+        uint4 v[2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const uint4*>(xr + xoff(u));
-        if (pun == 1.f && pend_un == 1.f) {   // the usual case: no rescaling of either half
+        for (int u = 0; u < 2; ++u) v[u] = *reinterpret_cast<const uint4*>(xr + xoff(u));
+        const uint32_t pw[8] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w};
+        if (pun == 1.f && pend_un == 1.f) {   // the usual case: no rescaling of either side
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t pw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t ow = pend[4 * u + e];
-              s[8 * u + 2 * e] = f16_lo(ow) + f16_lo(pw[e]);
-              s[8 * u + 2 * e + 1] = f16_hi(ow) + f16_hi(pw[e]);
-            }
+          for (int e = 0; e < 8; ++e) {
+            const float2 v2 = add_f16x2_f32(pend[e], pw[e]);
+            s[2 * e] = v2.x;
+            s[2 * e + 1] = v2.y;
           }
         } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t pw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t ow = pend[4 * u + e];
-              s[8 * u + 2 * e] = f16_lo(ow) * pend_un + f16_lo(pw[e]) * pun;
-              s[8 * u + 2 * e + 1] = f16_hi(ow) * pend_un + f16_hi(pw[e]) * pun;
-            }
+          for (int e = 0; e < 8; ++e) {
+            s[2 * e] = f16_lo(pend[e]) * pend_un + f16_lo(pw[e]) * pun;
+            s[2 * e + 1] = f16_hi(pend[e]) * pend_un + f16_hi(pw[e]) * pun;
           }
         }
       }
-      const int vh = valid - 32 * half;          // valid columns of this half
-      if (vh < 32) {
+      const int vh = valid - kCols * part;        // valid columns of this thread
+      if (vh < kCols) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) if (c >= vh) s[c] = -INFINITY;
+        for (int c = 0; c < kCols; ++c) if (c >= vh) s[c] = -INFINITY;
       }
       float mx;
       {
-        float t8[8];
+        float t4[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) t8[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
-        mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        for (int c = 0; c < 4; ++c) t4[c] = fmaxf(fmaxf(s[c], s[c + 4]), fmaxf(s[c + 8], s[c + 12]));
+        mx = fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3]));
       }
-      S->red[q & 1][half][h] = mx;
+      // row maximum over the kParts warps holding this row
+      S->red[q & 1][part][h] = mx;
       tc::mbar_arrive(&S->pair_max[quarter][q & 1]);
       if (!tc::mbar_wait(&S->pair_max[quarter][q & 1], (q >> 1) & 1)) return false;
-      mx = fmaxf(mx, S->red[q & 1][half ^ 1][h]) * sl;
+#pragma unroll
+      for (int pp = 0; pp < kParts; ++pp) mx = fmaxf(mx, S->red[q & 1][pp][h]);
+      mx *= sl;
       bool rescale = false;
       float alpha = 1.f;
       if (m_used == -INFINITY) {
@@ -655,21 +729,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
         rescale = true;
       }
       const float neg_m = -m_used;
-      uint32_t p[16];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t p[kCols / 2];
+      float ps[2] = {0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
+      for (int c = 0; c < kCols; c += 2) {
         const uint32_t w = tc::pack_bf16(tc::ex2_approx(fmaf(s[c], sl, neg_m)), tc::ex2_approx(fmaf(s[c + 1], sl, neg_m)));
         p[c / 2] = w;
-        ps[(c / 2) & 3] += bf_lo(w) + bf_hi(w);
+        ps[(c / 2) & 1] += bf_lo(w) + bf_hi(w);
       }
-      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      l += psum;
+      l += ps[0] + ps[1];
       // PV of the previous tile must be done: the P buffer and O are ours
       if (q > 0 && !tc::mbar_wait(&S->o_done, (q - 1) & 1)) return false;
       tc::tc_fence_after();
       if (rescale) {
-        for (int c0 = 0; c0 < 128; c0 += 16) {
+        for (int c0 = 0; c0 < 256 / kParts; c0 += 16) {
           uint32_t r[16];
           tc::tmem_ld16(t_o + c0, r);
           tc::tmem_ld_wait();
@@ -678,16 +751,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
           tc::tmem_st16(t_o + c0, r);
         }
       }
-      tc::tmem_st16(t_p, p);   // completed by finish_commit, after this tile's send
+      tc::tmem_st8(t_p, p);   // completed by finish_commit, after this tile's send
       return true;
     };
+
+    // FP8 cache: tile q's raw rows -> bf16 tile in the latent stage (128-byte swizzled
+    // boxes of 64 latent columns), value = E4M3 code * block scale rounded to bf16.
+    // 2,048 output chunks of 8 values per tile, four per softmax thread.
+    auto dequant = [&](uint32_t q) -> bool {
+      const uint32_t ws = q % kRawStages, st = q % kSt;
+      if (!tc::mbar_wait(&S->raw_full[ws], (q / kRawStages) & 1)) return false;
+      if (q >= static_cast<uint32_t>(kSt) && !tc::mbar_wait(&S->empty[st], ((q / kSt) - 1) & 1)) return false;
+      const uint8_t* raw = rawb + ws * kRawBytes;
+      uint8_t* stage = tiles + st * kStageBytes;
+#pragma unroll
+      for (int u = 0; u < (kTile * 32) / kSoftmaxThreads; ++u) {
+        const int ci = static_cast<int>(threadIdx.x) - 128 + u * kSoftmaxThreads;
+        const int row = ci >> 5, k = ci & 31;   // output chunk k = latent 8k..8k+7 of this CTA's 256
+        const uint2 codes = *reinterpret_cast<const uint2*>(raw + row * 256 + 8 * k);
+        const float sc = reinterpret_cast<const float*>(raw + kRawCodeBytes + row * 16)[2 * rank + (k >> 4)];
+        const uint32_t cw[2] = {codes.x, codes.y};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint16_t pair = static_cast<uint16_t>(cw[i >> 1] >> (16 * (i & 1)));
+          uint32_t h2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+          const float2 v = add_f16x2_f32(h2, 0u);
+          o[i] = tc::pack_bf16(v.x * sc, v.y * sc);
+        }
+        *reinterpret_cast<uint4*>(stage + (k >> 3) * kBlk + row * 128 + (((k & 7) ^ (row & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&S->full[st]);
+      tc::mbar_arrive(&S->raw_empty[ws]);
+      return true;
+    };
+    const uint32_t n_share = static_cast<uint32_t>(a.plan.share_start[cl + 1] - a.plan.share_start[cl]);
+    if (kF8 && n_share > 0 && !dequant(0)) ok = false;
 
     // Completes tile `q`: its P store, the rows past the sequence end, the hand-off to the PV warp.
     auto finish_commit = [&](uint32_t q, int valid) {
       tc::tmem_st_wait();
       // rows past the sequence end must not reach PV as NaN/Inf garbage
       if (valid < kTile) {
-        uint8_t* stage = tiles + (q % kStages) * kStageBytes;
+        uint8_t* stage = tiles + (q % kSt) * kStageBytes;
         const int nrow = kTile - valid;
         for (int idx = threadIdx.x - 128; idx < nrow * 4 * 8; idx += kSoftmaxThreads) {
           const int blk = idx / (nrow * 8), rem = idx % (nrow * 8);
@@ -709,50 +818,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       m_used = -INFINITY;
       l = 0.f;
       for (int j = j0; j < j1 && ok; ++j, ++it) {
-        // ---- own partial scores of tile it -> bf16 -> the peer
+        // ---- own partial scores of tile it -> scaled fp16 -> the peer
         ok = tc::mbar_wait(&S->s_full, it & 1);
         if (!ok || aborted(S)) { ok = false; break; }
         tc::tc_fence_after();
-        uint32_t own[16];
+        uint32_t own[kCols / 2];
         float own_un;
         {
-          uint32_t r0[16], r1[16];
+          uint32_t r0[16];
           tc::tmem_ld16(t_s, r0);
-          tc::tmem_ld16(t_s + 16, r1);
           tc::tmem_ld_wait();
           // columns past the sequence end hold scores of whatever the pool rows contain:
           // zero them so they cannot set the scale (the softmax masks them anyway)
-          const int vh = min(kTile, L - j * kTile) - 32 * half;
-          if (vh < 32) {
+          const int vh = min(kTile, L - j * kTile) - kCols * part;
+          if (vh < kCols) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              if (c >= vh) r0[c] = 0u;
-              if (16 + c >= vh) r1[c] = 0u;
-            }
+            for (int c = 0; c < 16; ++c) if (c >= vh) r0[c] = 0u;
           }
-          float am[8];
+          float am[4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            am[c] = fmaxf(fmaxf(fabsf(__uint_as_float(r0[2 * c])), fabsf(__uint_as_float(r0[2 * c + 1]))),
-                          fmaxf(fabsf(__uint_as_float(r1[2 * c])), fabsf(__uint_as_float(r1[2 * c + 1]))));
-          const float amax = fmaxf(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])),
-                                   fmaxf(fmaxf(am[4], am[5]), fmaxf(am[6], am[7])));
-          const float sc = exchange_scale(amax, &own_un);
+          for (int c = 0; c < 4; ++c)
+            am[c] = fmaxf(fmaxf(fabsf(__uint_as_float(r0[c])), fabsf(__uint_as_float(r0[c + 4]))),
+                          fmaxf(fabsf(__uint_as_float(r0[c + 8])), fabsf(__uint_as_float(r0[c + 12]))));
+          const float sc = exchange_scale(fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])), &own_un);
           if (sc != 1.f) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              r0[c] = __float_as_uint(__uint_as_float(r0[c]) * sc);
-              r1[c] = __float_as_uint(__uint_as_float(r1[c]) * sc);
-            }
+            for (int c = 0; c < 16; ++c) r0[c] = __float_as_uint(__uint_as_float(r0[c]) * sc);
           }
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            own[c] = pack_f16(__uint_as_float(r0[2 * c]), __uint_as_float(r0[2 * c + 1]));
-            own[8 + c] = pack_f16(__uint_as_float(r1[2 * c]), __uint_as_float(r1[2 * c + 1]));
-          }
+          for (int c = 0; c < 8; ++c) own[c] = pack_f16(__uint_as_float(r0[2 * c]), __uint_as_float(r0[2 * c + 1]));
         }
         tc::tc_fence_before();
         tc::mbar_arrive(&S->s_free);
+        if (kF8 && it + 1 < n_share && !dequant(it + 1)) { ok = false; break; }
         // ---- finish the previous tile of this segment (its peer half arrived while
         // this tile's scores were computed), then send this tile's half. Sending
         // only after consuming the peer's previous tile keeps two buffers safe:
@@ -766,14 +864,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
           const uint32_t dst = peer_x + xb * kXbufBytes;
           const uint32_t bar = xb ? peer_bar1 : peer_bar0;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 2; ++u)
             tc::st_async_v4(dst + xoff(u), bar, own[4 * u], own[4 * u + 1], own[4 * u + 2], own[4 * u + 3]);
-          tc::st_async_b32(dst + kXvalBytes + 4 * (half * kH + h), bar, __float_as_uint(own_un));
+          tc::st_async_b32(dst + kXvalBytes + 4 * (part * kH + h), bar, __float_as_uint(own_un));
         }
         if (have_pend) finish_commit(pend_it, pend_valid);
         if (j == j1 - 1 && have_next) load_q(nb_);   // all score MMAs of this segment are done
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pend[c] = own[c];
+        for (int c = 0; c < kCols / 2; ++c) pend[c] = own[c];
         pend_un = own_un;
         pend_valid = min(kTile, L - j * kTile);
         pend_it = it;
@@ -784,43 +882,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kAttendThreads, 1)
       have_pend = false;
       if (!ok) break;
       finish_commit(pend_it, pend_valid);
-      // ---- segment epilogue: unnormalised O half, m and l
+      // ---- segment epilogue: unnormalised O (this thread's 256 / kParts columns), m and l
       ok = tc::mbar_wait(&S->o_done, (it - 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
-      const int chunk0 = (rank * 256 + 128 * half) / 4;   // first 4-float chunk of this thread's columns
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 64) {
+      const int chunk0 = (rank * 256 + (256 / kParts) * part) / 4;   // first 4-float chunk of this thread's columns
+      {
         uint32_t r0[16], r1[16], r2[16], r3[16];
-        tc::tmem_ld16(t_o + c0, r0);
-        tc::tmem_ld16(t_o + c0 + 16, r1);
-        tc::tmem_ld16(t_o + c0 + 32, r2);
-        tc::tmem_ld16(t_o + c0 + 48, r3);
+        tc::tmem_ld16(t_o, r0);
+        tc::tmem_ld16(t_o + 16, r1);
+        tc::tmem_ld16(t_o + 32, r2);
+        tc::tmem_ld16(t_o + 48, r3);
         tc::tmem_ld_wait();
-        const int ch = chunk0 + c0 / 4;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + u, h)) =
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, chunk0 + u, h)) =
               make_uint4(r0[4 * u], r0[4 * u + 1], r0[4 * u + 2], r0[4 * u + 3]);
-          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + 4 + u, h)) =
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, chunk0 + 4 + u, h)) =
               make_uint4(r1[4 * u], r1[4 * u + 1], r1[4 * u + 2], r1[4 * u + 3]);
-          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + 8 + u, h)) =
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, chunk0 + 8 + u, h)) =
               make_uint4(r2[4 * u], r2[4 * u + 1], r2[4 * u + 2], r2[4 * u + 3]);
-          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, ch + 12 + u, h)) =
+          *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, chunk0 + 12 + u, h)) =
               make_uint4(r3[4 * u], r3[4 * u + 1], r3[4 * u + 2], r3[4 * u + 3]);
         }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&S->o_free);
-      // l of the two halves (both scaled by the same factors)
-      S->redl[half][h] = l;
+      // l of the kParts warps of this row (all scaled by the same factors)
+      S->redl[part][h] = l;
       tc::mbar_arrive(&S->pair_sum[quarter]);
       ok = tc::mbar_wait(&S->pair_sum[quarter], n_epi & 1);
       ++n_epi;
       if (!ok) break;
-      if (rank == 0 && half == 0) {
+      if (rank == 0 && part == 0) {
+        float lt = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < kParts; ++pp) lt += S->redl[pp][h];
         float2* ml = reinterpret_cast<float2*>(a.part_ml) + static_cast<int64_t>(slot) * kH + h;
-        *ml = make_float2(m_used, l + S->redl[1][h]);
+        *ml = make_float2(m_used, lt);
       }
       have = si.next(cum, a.batch, &b, &j0, &j1);
     }
@@ -846,10 +945,9 @@ struct MergeArgs {
   int batch, ncl;
 };
 
-constexpr int kMergeChunks = 1;                  // 4-float chunks per CTA (4 latent elements)
-constexpr int kMergeSplit = kOChunks / kMergeChunks;   // CTAs per sequence
+constexpr int kMergeSplit = kOChunks;            // CTAs per sequence: one 4-float chunk each
 
-// One CTA per (sequence b, 16 latent elements); thread = head. o_lat =
+// One CTA per (sequence b, 4 latent elements); thread = head. o_lat =
 // sum_s w_s O_s / sum_s w_s l_s with w_s = 2^(m_s - max m) over the partials
 // of b's segments (slots b + c for the clusters c whose shares meet b's
 // tiles). Every load is a warp reading 32 consecutive heads of one chunk.
@@ -858,58 +956,57 @@ __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int h = threadIdx.x;
   const int b = blockIdx.y;
-  const int chunk0 = blockIdx.x * kMergeChunks;
+  const int chunk = blockIdx.x;
   const int c0 = a.plan.seq_c0[b], c1 = a.plan.seq_c1[b];   // c1 < c0: no tiles, output 0
   const int32_t* start = a.plan.share_start;
-  float4 acc[kMergeChunks];
+  const float2* ml_all = reinterpret_cast<const float2*>(a.part_ml);
+  // online log-sum-exp over the partials, eight at a time so their loads overlap
+  float M = -INFINITY, den = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cb = c0; cb <= c1; cb += 8) {
+    float4 o[8];
+    float2 ml[8];
+    bool use[8];
 #pragma unroll
-  for (int k = 0; k < kMergeChunks; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (c1 >= c0) {
-    const float2* ml_all = reinterpret_cast<const float2*>(a.part_ml);
-    // running max and denominator in one pass
-    float M = -INFINITY, den = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-      if (start[c] == start[c + 1]) continue;   // empty share: no partial
-      const float2 ml = ml_all[static_cast<int64_t>(b + c) * kH + h];
-      if (ml.x > M) {
-        den = den * exp2f(M - ml.x) + ml.y;
-        M = ml.x;
+    for (int u = 0; u < 8; ++u) {
+      const int c = cb + u;
+      use[u] = c <= c1 && start[c] < start[c + 1];   // an empty share wrote no partial
+      if (use[u]) {
+        ml[u] = ml_all[static_cast<int64_t>(b + c) * kH + h];
+        o[u] = *reinterpret_cast<const float4*>(a.part_o + parto_index(b + c, chunk, h));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (!use[u]) continue;
+      float w = 1.f;
+      if (ml[u].x > M) {
+        const float r = exp2f(M - ml[u].x);   // 0 on the first partial (M = -inf)
+        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+        den *= r;
+        M = ml[u].x;
       } else {
-        den += exp2f(ml.x - M) * ml.y;
+        w = exp2f(ml[u].x - M);
       }
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll 2
-    for (int c = c0; c <= c1; ++c) {
-      if (start[c] == start[c + 1]) continue;
-      const float w = exp2f(ml_all[static_cast<int64_t>(b + c) * kH + h].x - M) * inv;
-      float4 v[kMergeChunks];
-#pragma unroll
-      for (int k = 0; k < kMergeChunks; ++k)
-        v[k] = *reinterpret_cast<const float4*>(a.part_o + parto_index(b + c, chunk0 + k, h));
-#pragma unroll
-      for (int k = 0; k < kMergeChunks; ++k) {
-        acc[k].x = fmaf(w, v[k].x, acc[k].x);
-        acc[k].y = fmaf(w, v[k].y, acc[k].y);
-        acc[k].z = fmaf(w, v[k].z, acc[k].z);
-        acc[k].w = fmaf(w, v[k].w, acc[k].w);
-      }
+      acc.x = fmaf(w, o[u].x, acc.x);
+      acc.y = fmaf(w, o[u].y, acc.y);
+      acc.z = fmaf(w, o[u].z, acc.z);
+      acc.w = fmaf(w, o[u].w, acc.w);
+      den = fmaf(w, ml[u].y, den);
     }
   }
-  const int64_t row = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * chunk0;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  const float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+  uint32_t hi[2], lo[2];
 #pragma unroll
-  for (int k = 0; k < kMergeChunks; ++k) {
-    const float v[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
-    uint32_t hi[2], lo[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
-      lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
-                            v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
-    }
-    *reinterpret_cast<uint2*>(a.o_hi + row + 4 * k) = make_uint2(hi[0], hi[1]);
-    *reinterpret_cast<uint2*>(a.o_lo + row + 4 * k) = make_uint2(lo[0], lo[1]);
+  for (int u = 0; u < 2; ++u) {
+    hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
+    lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
+                          v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
   }
+  const int64_t e = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * chunk;
+  *reinterpret_cast<uint2*>(a.o_hi + e) = make_uint2(hi[0], hi[1]);
+  *reinterpret_cast<uint2*>(a.o_lo + e) = make_uint2(lo[0], lo[1]);
 }
 
 // ================================================================== W_UV

@@ -163,8 +163,9 @@ mla_status decode_simt(const mla_config* c, const void* q_nope, const void* q_ro
 // and cache, and pages holding whole 64-token tiles.
 bool tc_supported(const mla_config* c) {
   return c->n_heads == tcd::kH && c->d_c == tcd::kDc && c->d_rope == tcd::kDr && c->d_head == tcd::kDh &&
-         c->io_dtype == MLA_DTYPE_BF16 && c->cache_dtype == MLA_DTYPE_BF16 && c->page_size % tcd::kTile == 0 &&
-         c->scale > 0.f;
+         c->io_dtype == MLA_DTYPE_BF16 &&
+         (c->cache_dtype == MLA_DTYPE_BF16 || c->cache_dtype == MLA_DTYPE_FP8_E4M3_B128) &&
+         c->page_size % tcd::kTile == 0 && c->scale > 0.f;
 }
 
 // Clusters the workspace is sized for; a launch never uses more.
@@ -206,21 +207,44 @@ TcPlan tc_plan(int batch) {
   return p;
 }
 
-constexpr size_t kAttendSmem = 1024 + tcd::kStages * tcd::kStageBytes + tcd::kRopeStages * tcd::kBlk +
-                               2 * tcd::kXbufBytes + sizeof(tcd::AttendSmem);
-static_assert(kAttendSmem <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
+template <bool kF8>
+constexpr size_t attend_smem() {
+  return 1024 + tcd::AttendLayout<kF8>::kXbuf + 2 * tcd::kXbufBytes + sizeof(tcd::AttendSmem);
+}
+static_assert(attend_smem<false>() <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
+static_assert(attend_smem<true>() <= 232448, "attend kernel (FP8 cache) shared memory exceeds 227 KB");
 constexpr size_t kUvSmem = 1024 + tcd::kUvSmem;
 size_t absorb_smem(int nb) { return 1024 + 4 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
 
 struct TcDeviceState {
   bool ready = false;
-  int clusters = 0;
+  int clusters[2] = {0, 0};   // bf16 cache, FP8 cache
 };
 std::mutex g_tc_mu;
 TcDeviceState g_tc_state[64];
 
-// Per device, once: shared-memory limits of the three kernels and the number
-// of two-CTA clusters of the attend kernel that fit on the GPU at once.
+template <bool kF8>
+mla_status attend_setup(int* clusters) {
+  const void* fn = reinterpret_cast<const void*>(tcd::attend_tc_kernel<kF8>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(attend_smem<kF8>()));
+  if (e != cudaSuccess) return cuda_fail(e, "attend smem attribute");
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(2 * kMaxClusters);
+  lc.blockDim = dim3(tcd::kAttendThreads);
+  lc.dynamicSmemBytes = attend_smem<kF8>();
+  int n = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&n, fn, &lc)) != cudaSuccess || n < 1)
+    return cuda_fail(e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "attend cluster occupancy");
+  const int half_sms = current_sm_count() / 2;
+  n = n < half_sms ? n : half_sms;
+  *clusters = n < kMaxClusters ? n : kMaxClusters;
+  return MLA_OK;
+}
+
+// Per device, once: shared-memory limits of the kernels and the number of
+// two-CTA clusters of each attend kernel that fit on the GPU at once.
+// clusters[0]: bf16 cache, clusters[1]: FP8 cache.
 mla_status tc_device_setup(int* clusters) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -232,25 +256,16 @@ mla_status tc_device_setup(int* clusters) {
     if ((e = cudaFuncSetAttribute(tcd::absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(absorb_smem(128)))) != cudaSuccess)
       return cuda_fail(e, "absorb smem attribute");
-    if ((e = cudaFuncSetAttribute(tcd::attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kAttendSmem))) != cudaSuccess)
-      return cuda_fail(e, "attend smem attribute");
     if ((e = cudaFuncSetAttribute(tcd::uv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kUvSmem))) != cudaSuccess)
       return cuda_fail(e, "uv smem attribute");
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(2 * kMaxClusters);
-    lc.blockDim = dim3(tcd::kAttendThreads);
-    lc.dynamicSmemBytes = kAttendSmem;
-    int n = 0;
-    if ((e = cudaOccupancyMaxActiveClusters(&n, tcd::attend_tc_kernel, &lc)) != cudaSuccess || n < 1)
-      return cuda_fail(e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "attend cluster occupancy");
-    const int half_sms = current_sm_count() / 2;
-    n = n < half_sms ? n : half_sms;
-    st.clusters = n < kMaxClusters ? n : kMaxClusters;
+    mla_status s = attend_setup<false>(&st.clusters[0]);
+    if (s != MLA_OK) return s;
+    if ((s = attend_setup<true>(&st.clusters[1])) != MLA_OK) return s;
     st.ready = true;
   }
-  *clusters = st.clusters;
+  clusters[0] = st.clusters[0];
+  clusters[1] = st.clusters[1];
   return MLA_OK;
 }
 
@@ -281,21 +296,42 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   if (pool_rows >= (static_cast<int64_t>(1) << 31))
     return fail(MLA_ERR_UNSUPPORTED, "pool of %lld rows exceeds the 2^31 rows a tile coordinate can address",
                 static_cast<long long>(pool_rows));
-  int ncl = 0;
-  mla_status s = tc_device_setup(&ncl);
+  const bool f8 = c->cache_dtype == MLA_DTYPE_FP8_E4M3_B128;
+  int ncl2[2] = {0, 0};
+  mla_status s = tc_device_setup(ncl2);
   if (s != MLA_OK) return s;
+  const int ncl = ncl2[f8 ? 1 : 0];
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   tcd::Plan plan{reinterpret_cast<int32_t*>(ws + p.off_lens), reinterpret_cast<int32_t*>(ws + p.off_cum),
                  reinterpret_cast<int32_t*>(ws + p.off_first), reinterpret_cast<int32_t*>(ws + p.off_start),
                  reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
-  CUtensorMap m_pool, m_wuk, m_wuv, m_qn, m_hi, m_lo;
+  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo;
   uint16_t* o_hi = reinterpret_cast<uint16_t*>(ws + p.off_hi);
   uint16_t* o_lo = reinterpret_cast<uint16_t*>(ws + p.off_lo);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (!make_map_2d(&m_pool, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, tcd::kTile, SW) ||
+  bool maps_ok;
+  int rope_x;
+  if (f8) {
+    // FP8 row: 512 E4M3 codes, 4 fp32 block scales, 64 bf16 rope values (656 bytes)
+    const uint64_t rb = tcd::kDc + 4 * (tcd::kDc / 128) + 2 * tcd::kDr;
+    const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapSwizzle NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint8_t* rope_base = static_cast<const uint8_t*>(pool) + tcd::kDc + 4 * (tcd::kDc / 128);
+    maps_ok = make_map_2d(&m_lat, pool, U8, rb, static_cast<uint64_t>(pool_rows), rb, 256, tcd::kTile, NS) &&
+              make_map_2d(&m_scale, pool, U8, rb, static_cast<uint64_t>(pool_rows), rb, 16, tcd::kTile, NS) &&
+              make_map_2d(&m_rope, rope_base, BF, tcd::kDr, static_cast<uint64_t>(pool_rows), rb, 64, tcd::kTile, SW);
+    rope_x = 0;
+  } else {
+    maps_ok = make_map_2d(&m_lat, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, tcd::kTile,
+                          SW);
+    m_scale = m_lat;
+    m_rope = m_lat;
+    rope_x = tcd::kDc;
+  }
+  if (!maps_ok ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
       !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
       !make_map_2d(&m_qn, q_nope, BF, tcd::kH * tcd::kDh, static_cast<uint64_t>(batch), tcd::kH * tcd::kDh * 2, 64,
@@ -326,6 +362,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   ta.batch = batch;
   ta.max_pages = max_pages;
   ta.page_size = c->page_size;
+  ta.rope_x = rope_x;
   ta.scale_log2 = c->scale * 1.4426950408889634f;
 
   tcd::MergeArgs ma{};
@@ -347,9 +384,11 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  absorb_smem(p.nb), st, absorb_args);
   if (s != MLA_OK) return s;
   stage_mark(1, st);
-  void* attend_args[] = {&m_pool, &ta};
-  s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_tc_kernel), dim3(2 * ncl), dim3(tcd::kAttendThreads),
-                 kAttendSmem, st, attend_args);
+  void* attend_args[] = {&m_lat, &m_scale, &m_rope, &ta};
+  s = launch_pdl(f8 ? reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>)
+                    : reinterpret_cast<const void*>(tcd::attend_tc_kernel<false>),
+                 dim3(2 * ncl), dim3(tcd::kAttendThreads), f8 ? attend_smem<true>() : attend_smem<false>(), st,
+                 attend_args);
   if (s != MLA_OK) return s;
   stage_mark(2, st);
   void* merge_args[] = {&ma};
