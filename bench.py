@@ -262,10 +262,17 @@ def run_gpu(args, rank, world, local):
         alg_bytes, alg_flop = weight_bytes / 2, 2 * B_ * H * shape.d_head * shape.d_c
     t = per_kernel[dom] / 1e3
     ach_gbs = alg_bytes / t / 1e9
-    roofline = {"bound": "hbm", "achieved": round(ach_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach_gbs / hbm, 4), "traffic": committed_traffic(dom), "kernel": dom,
-                "kernel_ms": round(per_kernel[dom], 5), "algorithmic_bytes": alg_bytes,
-                "tensor_tflops": round(alg_flop / t / 1e12, 1), "tensor_peak": tf_burst,
+    ach_tf = alg_flop / t / 1e12
+    # the kernel's bound is whichever of its bytes over HBM and its FLOPs over the tensor peak takes longer
+    tensor_bound = alg_flop / (tf_burst * 1e12) > alg_bytes / (hbm * 1e9)
+    roofline = {"bound": "tensor" if tensor_bound else "hbm",
+                "achieved": round(ach_tf if tensor_bound else ach_gbs, 1),
+                "peak": tf_burst if tensor_bound else hbm, "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                "frac": round(ach_tf / tf_burst if tensor_bound else ach_gbs / hbm, 4),
+                "traffic": committed_traffic(dom), "kernel": dom,
+                "kernel_ms": round(per_kernel[dom], 5), "algorithmic_bytes": alg_bytes, "algorithmic_flop": alg_flop,
+                "hbm_gbs": round(ach_gbs, 1), "hbm_peak": hbm, "tensor_tflops": round(ach_tf, 1),
+                "tensor_peak": tf_burst,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind,
                 "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()}}
     # whole-step roofline: the slower of all bytes over HBM and all FLOPs over the tensor peak

@@ -1,7 +1,9 @@
 // Tensor-core (tcgen05 + TMEM + TMA) MLA decode for the DeepSeek-V2 shape:
 // 128 heads of d_h = 128, latent d_c = 512, decoupled rope d_r = 64, bf16
-// queries and weights, bf16 cache rows of 576 values (DeepSeek-V2 report,
-// section 2.1.2 absorbed form, section 2.1.3 decoupled RoPE).
+// queries and weights; cache rows of 576 bf16 values, or 512 E4M3 codes with
+// an fp32 scale per 128 values plus 64 bf16 rope values (DeepSeek-V2 report,
+// section 2.1.2 absorbed form, section 2.1.3 decoupled RoPE, section 3.2.3
+// quantised KV cache).
 //
 // Four kernels per decode:
 //   absorb  : Q_lat[b,i,0:512] = W_UK[i]^T q_nope[b,i] (one CTA per head, the
@@ -17,9 +19,11 @@
 //             it with its peer through distributed shared memory, runs the
 //             (identical) online softmax, and accumulates its half of O_lat
 //             in TMEM. Each segment ends in an unnormalised partial
-//             (O half, running max m, sum l).
-//   merge   : one warp per (sequence, head): log-sum-exp merge of the
-//             sequence's partials, o_lat written as bf16 hi + lo.
+//             (O half, running max m, sum l). With an FP8 cache the softmax
+//             warps also dequantise the next tile into the bf16 stage.
+//   merge   : one CTA per (sequence, 4 latent columns), thread = head:
+//             log-sum-exp merge of the sequence's partials, o_lat written as
+//             bf16 hi + lo.
 //   uv      : one CTA per head: out[b,i,:] = W_UV[i] (o_hi + o_lo) on the
 //             tensor cores (M = 128 output rows, N = sequences).
 #pragma once
@@ -45,7 +49,7 @@ constexpr int kCols = kTile / kParts;        // score columns per softmax thread
 constexpr int kXvalBytes = kH * kTile * 2;   // one partial score tile as fp16
 constexpr int kXbufBytes = kXvalBytes + kParts * kH * 4;   // + one power-of-two scale per (row, column part)
 constexpr int kSoftmaxThreads = 128 * kParts;   // 4 TMEM lane quarters x kParts column parts
-constexpr int kAttendThreads = 128 + kSoftmaxThreads;  // warp 0 TMA, warps 1-2 MMA, warps 4-11 softmax
+constexpr int kAttendThreads = 128 + kSoftmaxThreads;  // warp 0 TMA, warps 1-2 MMA, warps 4-19 softmax
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: O is rescaled only when the max grows by > 2^8
 
 // Shared-memory carve-up of the attend kernel (after 1 KB alignment), per cache format.
