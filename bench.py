@@ -85,6 +85,12 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def job_value(world: int, tokens_per_rank: int, steps: int, slowest_seconds: float) -> float:
+    """Whole-job throughput: every rank decodes its own replica of the workload (weak scaling),
+    so the job attends world * tokens_per_rank cached tokens per step, timed by the slowest rank."""
+    return world * tokens_per_rank * steps / slowest_seconds
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -237,7 +243,7 @@ def run_gpu(args, rank, world, local):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * tokens * args.steps / (total_ms / 1e3)
+    value = job_value(world, tokens, args.steps, total_ms / 1e3)
 
     # per-kernel durations (separate pass, same steps, events between the kernels)
     names = M.decode_stage_names(cfg)
@@ -301,7 +307,7 @@ def run_gpu(args, rank, world, local):
         if k >= args.warmup:
             e2e_s += time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world, dev)
-    e2e = {"value": world * tokens * args.steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e = {"value": job_value(world, tokens, args.steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_s / args.steps, 4)}
 
     res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
