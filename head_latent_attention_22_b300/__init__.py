@@ -279,3 +279,43 @@ def decode_static_scratch(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Te
 def check_device_errors(stream=None) -> None:
     """Wait for the stream and raise MLAError if a kernel flagged a bounds or timeout error."""
     _check(_load().mla_check_device_errors(_stream(stream)))
+
+
+class StepGraph:
+    """One serving step - mla_append of the new tokens, then mla_decode - captured once
+    into a CUDA graph and replayed.
+
+    The arguments are those of append() and decode(); every tensor must stay
+    allocated and in place while the graph lives, because the captured launches
+    hold their addresses (and the tensor maps built from them). replay() runs
+    the same kernels on whatever the tensors hold at that moment, on the current
+    stream: the caller writes the step's inputs into them, replays, and reads
+    `out`. Sizes (batch, max_seq_len, number of new tokens) are fixed at capture.
+    The constructor runs the step once eagerly before capturing it (writing the
+    new tokens' cache rows, which replaying rewrites with the same values).
+    """
+
+    def __init__(self, cfg: MLAConfig, *, c_new: torch.Tensor, k_new: torch.Tensor, positions: torch.Tensor,
+                 seq_idx: Optional[torch.Tensor], q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: torch.Tensor,
+                 w_uv: torch.Tensor, pool: torch.Tensor, block_table: Optional[torch.Tensor], seq_lens: torch.Tensor,
+                 max_seq_len: int, out: torch.Tensor, workspace: torch.Tensor, max_pages: Optional[int] = None):
+        batch = q_nope.shape[0]
+
+        def step():
+            append(cfg, c_new, k_new, positions, pool, block_table, seq_idx=seq_idx, batch=batch,
+                   max_pages=max_pages)
+            decode(cfg, q_nope, q_rope, w_uk, w_uv, pool, block_table, seq_lens, max_seq_len, out=out,
+                   workspace=workspace, max_pages=max_pages)
+
+        # one eager step first: the per-device setup of the library (kernel attributes, occupancy)
+        # happens on a first call and must not fall inside the capture
+        step()
+        check_device_errors()
+        self.out = out
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            step()
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.out
