@@ -137,17 +137,53 @@ def rope_inv_freq(d_rope: int, theta: float) -> np.ndarray:
     return np.power(float(theta), -2.0 * m / d_rope)
 
 
-def rope(x: np.ndarray, pos: np.ndarray, theta: float, interleaved: bool = True) -> np.ndarray:
+def yarn_ramp(r, alpha: float, beta: float):
+    """YaRN's ramp gamma(r) (Peng et al. 2023, the method section 3.1.4 applies):
+    0 below alpha, 1 above beta, linear in r between."""
+    r = np.asarray(r, dtype=np.float64)
+    return np.clip((r - alpha) / (beta - alpha), 0.0, 1.0)
+
+
+def yarn_inv_freq(d_rope: int, theta: float, s: float, alpha: float, beta: float, orig_len: int) -> np.ndarray:
+    """Rotation frequencies of the decoupled RoPE under YaRN (section 3.1.4: s = 40, alpha = 1,
+    beta = 32, extending a 4K context).
+
+    Pair m turns at theta_m = theta^(-2m/d), with wavelength 2 pi / theta_m; over the
+    original context it makes r = orig_len / wavelength turns. YaRN's "NTK-by-parts" rule
+    interpolates the slow pairs and keeps the fast ones:
+        h(theta_m) = (1 - gamma(r)) theta_m / s + gamma(r) theta_m.
+    s <= 1 leaves the frequencies as they are.
+    """
+    base = rope_inv_freq(d_rope, theta)
+    if s <= 1.0:
+        return base
+    r = orig_len * base / (2.0 * math.pi)
+    g = yarn_ramp(r, alpha, beta)
+    return (1.0 - g) * base / s + g * base
+
+
+def yarn_logit_factor(s: float, coeff: float = 0.0707) -> float:
+    """Multiplier t of the attention logits under YaRN: sqrt(t) = coeff ln s + 1 (section 3.1.4),
+    read as scaling both the query and the key by sqrt(t), as YaRN scales them; 1 for s <= 1."""
+    if s <= 1.0:
+        return 1.0
+    return (coeff * math.log(s) + 1.0) ** 2
+
+
+def rope(x: np.ndarray, pos: np.ndarray, theta: float, interleaved: bool = True,
+         inv_freq: Optional[np.ndarray] = None) -> np.ndarray:
     """Rotary position embedding of the decoupled key (RoFormer, cited in section 2.1.3).
 
     Pair m of a d-vector at position p turns by the angle p * theta^(-2m/d):
     (a, b) -> (a cos - b sin, a sin + b cos). interleaved=True pairs
     components (2m, 2m+1) as in RoFormer's definition; False pairs (m, m + d/2).
+    inv_freq replaces theta^(-2m/d) (YaRN: yarn_inv_freq).
     x: [..., d]; pos: broadcastable to x[..., 0].
     """
     x = np.asarray(x, dtype=np.float64)
     d = x.shape[-1]
-    ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(d, theta)
+    f = rope_inv_freq(d, theta) if inv_freq is None else np.asarray(inv_freq, dtype=np.float64)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * f
     c, s = np.cos(ang), np.sin(ang)
     if interleaved:
         a, b = x[..., 0::2], x[..., 1::2]
@@ -163,7 +199,7 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float, interleaved: bool = True)
 
 
 def append_rows(c_kv_raw, k_rope_raw, positions, *, cache_dtype: str, eps: float,
-                theta: float, interleaved: bool = True, gamma=None, block: int = 128):
+                theta: float, interleaved: bool = True, gamma=None, block: int = 128, inv_freq=None):
     """What one cache row holds after the append step, as fp64 values.
 
     c = RMSNorm(c_kv_raw) (sections 2.1.2 + 3.1.2) and kR = RoPE(k_rope_raw, pos)
@@ -174,7 +210,7 @@ def append_rows(c_kv_raw, k_rope_raw, positions, *, cache_dtype: str, eps: float
     E4M3 codes and scales for the fp8 format (else None).
     """
     c = rmsnorm(np.asarray(c_kv_raw, dtype=np.float64), eps, gamma)
-    kr = rope(np.asarray(k_rope_raw, dtype=np.float64), np.asarray(positions), theta, interleaved)
+    kr = rope(np.asarray(k_rope_raw, dtype=np.float64), np.asarray(positions), theta, interleaved, inv_freq)
     if cache_dtype == "fp32":
         return fp32(c).astype(np.float64), fp32(kr).astype(np.float64), None
     if cache_dtype == "bf16":

@@ -330,3 +330,66 @@ def test_yarn_entropy_factor():
     y = f["yarn"]
     assert O.yarn_mscale_sqrt_t(y["s"]) == pytest.approx(y["sqrt_t_coeff"] * math.log(40) + 1)
     assert O.yarn_mscale_sqrt_t(1.0) == 1.0
+
+
+# ---------------------------------------------------------------------------- YaRN (section 3.1.4)
+
+def _yarn_facts():
+    y = json.load(open(os.path.join(GOLDEN, "pages_facts.json")))["yarn"]
+    return y["s"], y["alpha"], y["beta"], y
+
+
+def test_yarn_scale_factor_matches_the_pages_contexts():
+    # the pages extend a 4K context with s = 40 to a 160K target
+    s, _, _, y = _yarn_facts()
+    assert int(y["orig_context"].rstrip("K")) * s == int(y["target_context"].rstrip("K"))
+
+
+def test_yarn_ramp_endpoints_continuity_and_monotonicity():
+    _, a, b, _ = _yarn_facts()
+    r = np.linspace(0.0, 2 * b, 20001)
+    g = O.yarn_ramp(r, a, b)
+    assert np.all(g[r <= a] == 0.0) and np.all(g[r >= b] == 1.0)
+    assert np.all(np.diff(g) >= 0.0)                        # never decreasing
+    assert np.max(np.abs(np.diff(g))) <= (r[1] - r[0]) / (b - a) + 1e-12   # no jump anywhere
+    assert O.yarn_ramp((a + b) / 2, a, b) == pytest.approx(0.5)
+
+
+def test_yarn_frequencies_interpolate_slow_pairs_and_keep_fast_ones():
+    s, a, b, _ = _yarn_facts()
+    d, theta, L = 64, 10000.0, 4096
+    base = O.rope_inv_freq(d, theta)
+    f = O.yarn_inv_freq(d, theta, s, a, b, L)
+    turns = L * base / (2 * math.pi)          # turns of each pair over the original context
+    slow, fast = turns < a, turns > b
+    assert slow.any() and fast.any() and (~slow & ~fast).any()   # the DeepSeek-V2 setting has all three regimes
+    # fast pairs (many turns over the original context) are left as they are
+    np.testing.assert_array_equal(f[fast], base[fast])
+    # slow pairs are position-interpolated: over the extended context s L they turn exactly
+    # as far as they used to over L
+    np.testing.assert_allclose(s * L * f[slow], L * base[slow], rtol=1e-13)
+    # in between, the slowdown factor lies strictly between 1/s and 1, and faster pairs are slowed less
+    mid = ~slow & ~fast
+    ratio = f / base
+    assert np.all((ratio[mid] > 1 / s) & (ratio[mid] < 1))
+    assert np.all(np.diff(ratio) <= 1e-15)    # pairs are ordered from fast (m = 0) to slow
+    # s <= 1 is plain RoPE
+    np.testing.assert_array_equal(O.yarn_inv_freq(d, theta, 1.0, a, b, L), base)
+
+
+def test_yarn_rope_keeps_norm_and_relative_position_property():
+    s, a, b, _ = _yarn_facts()
+    rng = np.random.default_rng(5)
+    f = O.yarn_inv_freq(64, 1e4, s, a, b, 4096)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    for m, n in [(100000, 99000), (5, 0), (131071, 130000)]:
+        qm, kn = O.rope(q, m, 1e4, inv_freq=f), O.rope(k, n, 1e4, inv_freq=f)
+        q2, k2 = O.rope(q, m + 777, 1e4, inv_freq=f), O.rope(k, n + 777, 1e4, inv_freq=f)
+        assert qm @ kn == pytest.approx(q2 @ k2, rel=1e-9, abs=1e-9)
+        assert np.linalg.norm(qm) == pytest.approx(np.linalg.norm(q))
+
+
+def test_yarn_logit_factor_is_the_square_of_the_pages_sqrt_t():
+    s, _, _, y = _yarn_facts()
+    assert O.yarn_logit_factor(s, y["sqrt_t_coeff"]) == pytest.approx(O.yarn_mscale_sqrt_t(s) ** 2)
+    assert O.yarn_logit_factor(1.0) == 1.0
