@@ -356,6 +356,8 @@ def oracle_sample(inp, seconds: float, step: int = 0):
     w_uk = inp.w_uk.double().numpy()
     w_uv = inp.w_uv.double().numpy()
     qn, qr = st.q_nope.double().numpy(), st.q_rope.double().numpy()
+    inv_freq = O.yarn_inv_freq(s.d_rope, s.rope_theta, s.yarn_factor, s.yarn_alpha, s.yarn_beta, s.yarn_orig_len)
+    scale = s.scale * O.yarn_logit_factor(s.yarn_factor, s.yarn_mscale)
     # cache content of the sequences the sample touches (not timed: it is resident state)
     order = [(int(b), int(i)) for b, i in zip(rng.integers(0, s.batch, 1 << 16), rng.integers(0, s.n_heads, 1 << 16))]
     seqs = sorted({b for b, _ in order[:64]})
@@ -363,18 +365,19 @@ def oracle_sample(inp, seconds: float, step: int = 0):
     for b in seqs:
         o0, o1 = int(inp.token_offsets[b]), int(inp.token_offsets[b + 1]) - 1
         c, kr, _ = O.append_rows(inp.c_kv_raw[o0:o1].double().numpy(), inp.k_rope_raw[o0:o1].double().numpy(),
-                                 np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta)
+                                 np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta,
+                                 inv_freq=inv_freq)
         cache[b] = (c, kr)
     t0 = time.perf_counter()
     c_new, k_new, _ = O.append_rows(st.c_new.double().numpy(), st.k_new.double().numpy(), inp.lengths - 1,
-                                    cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta)
+                                    cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta, inv_freq=inv_freq)
     done, tok = 0, 0
     for b, i in order:
         if b not in cache:
             continue
         c = np.concatenate([cache[b][0], c_new[b:b + 1]])
         kr = np.concatenate([cache[b][1], k_new[b:b + 1]])
-        O.head_absorbed(qn[b, i], qr[b, i], w_uk[i], w_uv[i], c, kr, s.scale)
+        O.head_absorbed(qn[b, i], qr[b, i], w_uk[i], w_uv[i], c, kr, scale)
         done += 1
         tok += len(c)
         if time.perf_counter() - t0 > seconds:

@@ -46,7 +46,9 @@ class _CConfig(ctypes.Structure):
     _fields_ = [("n_heads", ctypes.c_int32), ("d_c", ctypes.c_int32), ("d_rope", ctypes.c_int32),
                 ("d_head", ctypes.c_int32), ("page_size", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
                 ("cache_dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("eps", ctypes.c_float),
-                ("rope_theta", ctypes.c_float), ("rope_interleaved", ctypes.c_int32)]
+                ("rope_theta", ctypes.c_float), ("rope_interleaved", ctypes.c_int32),
+                ("yarn_factor", ctypes.c_float), ("yarn_alpha", ctypes.c_float), ("yarn_beta", ctypes.c_float),
+                ("yarn_mscale", ctypes.c_float), ("yarn_orig_len", ctypes.c_int32)]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -64,6 +66,11 @@ class MLAConfig:
     eps: float = 1e-6
     rope_theta: float = 10000.0
     rope_interleaved: bool = True
+    yarn_factor: float = 1.0    # YaRN scale s; <= 1: plain RoPE (DeepSeek-V2 long context: 40)
+    yarn_alpha: float = 1.0
+    yarn_beta: float = 32.0
+    yarn_mscale: float = 0.0707
+    yarn_orig_len: int = 4096
 
     @staticmethod
     def dsv2(cache_dtype: int = BF16, page_size: int = 64) -> "MLAConfig":
@@ -75,12 +82,15 @@ class MLAConfig:
         """From an object with the fields of a workload description (mla_synth.MLAShape)."""
         return MLAConfig(shape.n_heads, shape.d_c, shape.d_rope, shape.d_head, shape.page_size,
                          _DTYPE_NAMES[shape.io_dtype], _DTYPE_NAMES[shape.cache_dtype], float(shape.scale),
-                         float(shape.eps), float(shape.rope_theta), True)
+                         float(shape.eps), float(shape.rope_theta), True, float(shape.yarn_factor),
+                         float(shape.yarn_alpha), float(shape.yarn_beta), float(shape.yarn_mscale),
+                         int(shape.yarn_orig_len))
 
     def c(self) -> _CConfig:
         scale = self.scale if self.scale else 1.0 / math.sqrt(self.d_head + self.d_rope)
         return _CConfig(self.n_heads, self.d_c, self.d_rope, self.d_head, self.page_size, self.io_dtype,
-                        self.cache_dtype, scale, self.eps, self.rope_theta, int(self.rope_interleaved))
+                        self.cache_dtype, scale, self.eps, self.rope_theta, int(self.rope_interleaved),
+                        self.yarn_factor, self.yarn_alpha, self.yarn_beta, self.yarn_mscale, self.yarn_orig_len)
 
     @property
     def io_torch_dtype(self) -> torch.dtype:
@@ -110,6 +120,7 @@ def _load():
         "mla_decode_stage_names": (ctypes.c_char_p, [CFG]),
         "mla_decode_static_scratch": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, P, P]),
         "mla_set_stage_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
+        "mla_rope_query": (I32, [CFG, P, P, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -184,6 +195,22 @@ def append(cfg: MLAConfig, c_kv_raw: torch.Tensor, k_rope_raw: torch.Tensor, pos
     _check(_load().mla_append(ctypes.byref(cfg.c()), _ptr(c_kv_raw), _ptr(k_rope_raw), _ptr(positions),
                               _ptr(seq_idx), _ptr(gamma), _ptr(pool), pool.shape[0], _ptr(block_table),
                               batch, max_pages, T, _stream(stream)))
+
+
+def rope_query(cfg: MLAConfig, q_rope_raw: torch.Tensor, positions: torch.Tensor,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """mla_rope_query: the query's rope part rotated with the keys' frequencies (YaRN included)."""
+    _need(q_rope_raw, "q_rope_raw", cfg.io_torch_dtype, 3)
+    _need(positions, "positions", torch.int32, 1)
+    B = q_rope_raw.shape[0]
+    if q_rope_raw.shape != (B, cfg.n_heads, cfg.d_rope) or positions.shape[0] != B:
+        raise ValueError("q_rope_raw must be [batch, n_heads, d_rope] with one position per sequence")
+    if out is None:
+        out = torch.empty_like(q_rope_raw)
+    _need(out, "out", cfg.io_torch_dtype, 3)
+    _check(_load().mla_rope_query(ctypes.byref(cfg.c()), _ptr(q_rope_raw), _ptr(positions), _ptr(out), B,
+                                  _stream(stream)))
+    return out
 
 
 def workspace_size(cfg: MLAConfig, batch: int, max_seq_len: int) -> int:

@@ -9,6 +9,26 @@
 
 namespace mla {
 
+// Frequencies of the decoupled RoPE: f_m = theta^(-2m/d), and under YaRN (s > 1) the
+// "NTK-by-parts" rule of YaRN (Peng et al. 2023) that the DeepSeek-V2 report applies
+// (section 3.1.4): a pair making r = orig_len f / (2 pi) turns over the original context
+// keeps f for r >= beta, takes f / s for r <= alpha, and blends linearly in r between.
+struct RopeFreq {
+  double log_theta;
+  double yarn_s, yarn_alpha, yarn_beta, yarn_orig_len;   // yarn_s <= 1: plain RoPE
+};
+
+__device__ __forceinline__ double rope_freq(const RopeFreq& r, int m, int d_rope) {
+  double f = exp(-(2.0 * m / d_rope) * r.log_theta);
+  if (r.yarn_s > 1.0) {
+    const double turns = r.yarn_orig_len * f / (2.0 * 3.141592653589793);
+    double g = (turns - r.yarn_alpha) / (r.yarn_beta - r.yarn_alpha);
+    g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
+    f = (1.0 - g) * f / r.yarn_s + g * f;
+  }
+  return f;
+}
+
 struct AppendArgs {
   const void* c_raw;
   const void* k_raw;
@@ -20,7 +40,7 @@ struct AppendArgs {
   const int32_t* block_table;
   int batch, max_pages, n_tokens, d_c, d_rope, page_size, cache_dtype, rope_interleaved;
   float eps;
-  double log_theta;
+  RopeFreq rf;
   int64_t row_bytes;
 };
 
@@ -38,10 +58,10 @@ __device__ __forceinline__ int64_t append_slot(const AppendArgs& a, int t, int* 
   return page * a.page_size + pos % a.page_size;
 }
 
-// Rotation of pair m at position pos: angle pos * theta^(-2m/d) in fp64.
+// Rotation of pair m at position pos: angle pos * f_m in fp64.
 __device__ __forceinline__ void rope_pair(double a, double b, int m, int d_rope, int pos,
-                                          double log_theta, double* ra, double* rb) {
-  const double inv_freq = exp(-(2.0 * m / d_rope) * log_theta);
+                                          const RopeFreq& rf, double* ra, double* rb) {
+  const double inv_freq = rope_freq(rf, m, d_rope);
   double sn, cs;
   sincos(static_cast<double>(pos) * inv_freq, &sn, &cs);
   *ra = a * cs - b * sn;
@@ -131,7 +151,7 @@ __global__ void __launch_bounds__(256) append_dsv2_kernel(AppendArgs a) {
   const int i0 = a.rope_interleaved ? 2 * lane : lane;
   const int i1 = a.rope_interleaved ? 2 * lane + 1 : lane + 32;
   double ra, rb;
-  rope_pair(bf16_to_f32(kr[i0]), bf16_to_f32(kr[i1]), lane, 64, pos, a.log_theta, &ra, &rb);
+  rope_pair(bf16_to_f32(kr[i0]), bf16_to_f32(kr[i1]), lane, 64, pos, a.rf, &ra, &rb);
   if (a.rope_interleaved) {
     *reinterpret_cast<uint32_t*>(kdst + i0) =
         static_cast<uint32_t>(f64_to_bf16_bits(ra)) | (static_cast<uint32_t>(f64_to_bf16_bits(rb)) << 16);
@@ -195,13 +215,53 @@ __global__ void __launch_bounds__(256) append_generic_kernel(AppendArgs a) {
     const int i0 = a.rope_interleaved ? 2 * m : m;
     const int i1 = a.rope_interleaved ? 2 * m + 1 : m + half;
     double ra, rb;
-    rope_pair(load_as_f32(k, i0), load_as_f32(k, i1), m, a.d_rope, pos, a.log_theta, &ra, &rb);
+    rope_pair(load_as_f32(k, i0), load_as_f32(k, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
     if (a.cache_dtype == MLA_DTYPE_FP32) {
       float* dst = reinterpret_cast<float*>(row + rope_off);
       dst[i0] = static_cast<float>(ra);
       dst[i1] = static_cast<float>(rb);
     } else {
       uint16_t* dst = reinterpret_cast<uint16_t*>(row + rope_off);
+      dst[i0] = f64_to_bf16_bits(ra);
+      dst[i1] = f64_to_bf16_bits(rb);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- mla_rope_query
+// q_rope[b, i, :] = RoPE(q_rope_raw[b, i, :], positions[b]) with the frequencies of
+// the keys; one thread per (row, pair), so the rotation may be done in place.
+struct RopeQueryArgs {
+  const void* in;
+  void* out;
+  const int32_t* positions;
+  int batch, n_heads, d_rope, rope_interleaved;
+  RopeFreq rf;
+};
+
+template <typename T>
+__global__ void rope_query_kernel(RopeQueryArgs a) {
+  const int half = a.d_rope / 2;
+  const int64_t n = static_cast<int64_t>(a.batch) * a.n_heads * half;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(idx % half);
+    const int64_t row = idx / half;   // b * n_heads + i
+    const int pos = a.positions[row / a.n_heads];
+    if (pos < 0) {
+      if (m == 0) flag_error(ERR_BIT_BOUNDS);
+      continue;
+    }
+    const int i0 = a.rope_interleaved ? 2 * m : m;
+    const int i1 = a.rope_interleaved ? 2 * m + 1 : m + half;
+    const T* src = static_cast<const T*>(a.in) + row * a.d_rope;
+    T* dst = static_cast<T*>(a.out) + row * a.d_rope;
+    double ra, rb;
+    rope_pair(load_as_f32(src, i0), load_as_f32(src, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
+    if constexpr (sizeof(T) == 4) {
+      dst[i0] = static_cast<float>(ra);
+      dst[i1] = static_cast<float>(rb);
+    } else {
       dst[i0] = f64_to_bf16_bits(ra);
       dst[i1] = f64_to_bf16_bits(rb);
     }

@@ -59,7 +59,34 @@ mla_status check_config(const mla_config* c) {
     return fail(MLA_ERR_INVALID_ARG, "FP8 cache needs d_c %% 128 == 0 (d_c=%d)", c->d_c);
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f) || !std::isfinite(c->scale))
     return fail(MLA_ERR_INVALID_ARG, "bad eps/rope_theta/scale");
+  if (c->yarn_factor > 1.f &&
+      (!std::isfinite(c->yarn_factor) || !(c->yarn_beta > c->yarn_alpha) || !std::isfinite(c->yarn_alpha) ||
+       !std::isfinite(c->yarn_beta) || !std::isfinite(c->yarn_mscale) || c->yarn_orig_len < 1))
+    return fail(MLA_ERR_INVALID_ARG, "bad YaRN fields: factor=%g alpha=%g beta=%g mscale=%g orig_len=%d",
+                c->yarn_factor, c->yarn_alpha, c->yarn_beta, c->yarn_mscale, c->yarn_orig_len);
   return MLA_OK;
+}
+
+bool yarn_on(const mla_config* c) { return c->yarn_factor > 1.f; }
+
+// RoPE frequencies of cfg (plain, or YaRN-scaled), as the kernels take them.
+RopeFreq rope_freq_of(const mla_config* c) {
+  RopeFreq r{};
+  r.log_theta = std::log(static_cast<double>(c->rope_theta));
+  if (yarn_on(c)) {
+    r.yarn_s = c->yarn_factor;
+    r.yarn_alpha = c->yarn_alpha;
+    r.yarn_beta = c->yarn_beta;
+    r.yarn_orig_len = c->yarn_orig_len;
+  }
+  return r;
+}
+
+// Softmax scale of the decode: cfg->scale, times YaRN's logit factor (mscale ln s + 1)^2.
+float softmax_scale(const mla_config* c) {
+  if (!yarn_on(c)) return c->scale;
+  const double m = static_cast<double>(c->yarn_mscale) * std::log(static_cast<double>(c->yarn_factor)) + 1.0;
+  return static_cast<float>(static_cast<double>(c->scale) * m * m);
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -121,7 +148,7 @@ mla_status decode_simt(const mla_config* c, const void* q_nope, const void* q_ro
   a.d_rope = c->d_rope; a.d_head = c->d_head; a.page_size = c->page_size;
   a.cache_dtype = c->cache_dtype;
   a.row_bytes = static_cast<int64_t>(row_bytes_of(c->cache_dtype, c->d_c, c->d_rope));
-  a.scale_log2 = c->scale * 1.4426950408889634f;
+  a.scale_log2 = softmax_scale(c) * 1.4426950408889634f;
   a.out = out;
   a.q_lat = reinterpret_cast<float*>(ws + p.off_qlat);
   a.part_o = reinterpret_cast<float*>(ws + p.off_o);
@@ -363,7 +390,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   ta.max_pages = max_pages;
   ta.page_size = c->page_size;
   ta.rope_x = rope_x;
-  ta.scale_log2 = c->scale * 1.4426950408889634f;
+  ta.scale_log2 = softmax_scale(c) * 1.4426950408889634f;
 
   tcd::MergeArgs ma{};
   ma.plan = plan;
@@ -461,7 +488,7 @@ mla_status mla_append(const mla_config* cfg, const void* c_kv_raw, const void* k
   a.pool = static_cast<uint8_t*>(pool); a.num_pages = num_pages; a.block_table = block_table;
   a.batch = batch; a.max_pages = max_pages; a.n_tokens = n_tokens; a.d_c = cfg->d_c; a.d_rope = cfg->d_rope;
   a.page_size = cfg->page_size; a.cache_dtype = cfg->cache_dtype; a.rope_interleaved = cfg->rope_interleaved;
-  a.eps = cfg->eps; a.log_theta = std::log(static_cast<double>(cfg->rope_theta));
+  a.eps = cfg->eps; a.rf = rope_freq_of(cfg);
   a.row_bytes = static_cast<int64_t>(row_bytes_of(cfg->cache_dtype, cfg->d_c, cfg->d_rope));
   const cudaStream_t st = as_stream(stream);
   const int threads = 256, warps = threads / 32;
@@ -485,6 +512,36 @@ size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, int32_t m
   if (check_config(cfg) != MLA_OK || batch < 1) return 0;
   if (tc_supported(cfg)) return tc_plan(batch).bytes;
   return simt_plan(cfg, batch, max_seq_len).bytes;
+}
+
+mla_status mla_rope_query(const mla_config* cfg, const void* q_rope_raw, const int32_t* positions, void* q_rope,
+                          int32_t batch, void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (batch < 0) return fail(MLA_ERR_INVALID_ARG, "batch=%d", batch);
+  if (batch == 0) return MLA_OK;
+  if (!q_rope_raw || !positions || !q_rope) return fail(MLA_ERR_INVALID_ARG, "NULL argument");
+  RopeQueryArgs a{};
+  a.in = q_rope_raw;
+  a.out = q_rope;
+  a.positions = positions;
+  a.batch = batch;
+  a.n_heads = cfg->n_heads;
+  a.d_rope = cfg->d_rope;
+  a.rope_interleaved = cfg->rope_interleaved;
+  a.rf = rope_freq_of(cfg);
+  const int64_t n = static_cast<int64_t>(batch) * cfg->n_heads * (cfg->d_rope / 2);
+  const int threads = 256;
+  const int64_t want = (n + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+  const cudaStream_t st = as_stream(stream);
+  if (cfg->io_dtype == MLA_DTYPE_BF16)
+    rope_query_kernel<uint16_t><<<blocks, threads, 0, st>>>(a);
+  else
+    rope_query_kernel<float><<<blocks, threads, 0, st>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "rope_query launch");
+  return MLA_OK;
 }
 
 int32_t mla_decode_path(const mla_config* cfg) {

@@ -74,6 +74,19 @@ typedef struct {
   float eps;                /* RMSNorm epsilon */
   float rope_theta;         /* RoPE base; pair m turns by pos * theta^(-2m/d_rope) */
   int32_t rope_interleaved; /* 1: pairs (2m, 2m+1) (RoFormer); 0: pairs (m, m + d_rope/2) */
+  /* YaRN extension of the decoupled RoPE (report section 3.1.4; there s = 40,
+     alpha = 1, beta = 32 over a 4K context, mscale 0.0707). yarn_factor s > 1
+     turns it on; <= 1 means plain RoPE and the other yarn fields are ignored.
+     Pair m's frequency f = rope_theta^(-2m/d_rope) makes r = yarn_orig_len f / (2 pi)
+     turns over the original context and becomes (1 - g) f / s + g f with
+     g = clamp((r - yarn_alpha) / (yarn_beta - yarn_alpha), 0, 1) in mla_append and
+     mla_rope_query; mla_decode multiplies the logits by (yarn_mscale ln s + 1)^2
+     on top of `scale`. */
+  float yarn_factor;
+  float yarn_alpha;
+  float yarn_beta;
+  float yarn_mscale;
+  int32_t yarn_orig_len;
 } mla_config;
 
 /* Bytes of one cache row for `cfg` (0 if cfg is invalid):
@@ -195,6 +208,19 @@ MLA_API mla_status mla_decode_static_scratch(const mla_config* cfg, const void* 
  * word: MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (timeout wins if both).
  */
 MLA_API mla_status mla_check_device_errors(void* stream);
+
+/*
+ * mla_rope_query - rotate the rope part of the decode queries (report section
+ * 2.1.3: q^R = RoPE(W_QR c^Q)) with the frequencies mla_append gives the keys,
+ * YaRN included:
+ *   q_rope[b, i, :] = RoPE(q_rope_raw[b, i, :], positions[b])
+ * angle and rotation in fp64, the result rounded to nearest even in io_dtype.
+ *   q_rope_raw, q_rope [batch, n_heads, d_rope] io_dtype (may be the same array)
+ *   positions          [batch] int32, the position of each sequence's query token
+ * A negative position skips the sequence's rows and sets MLA_ERR_BOUNDS.
+ */
+MLA_API mla_status mla_rope_query(const mla_config* cfg, const void* q_rope_raw, const int32_t* positions,
+                                  void* q_rope, int32_t batch, void* stream);
 
 /* Which kernels mla_decode would use for cfg on the current device:
    1 = tcgen05/TMA tensor-core path, 0 = CUDA-core (SIMT) path. */

@@ -53,6 +53,11 @@ class MLAShape:
     paged: bool = True                # False => contiguous [B, max_seq] layout
     eps: float = 1e-6
     rope_theta: float = 10000.0
+    yarn_factor: float = 1.0          # YaRN scale s of the decoupled RoPE; <= 1: plain RoPE
+    yarn_alpha: float = 1.0
+    yarn_beta: float = 32.0
+    yarn_mscale: float = 0.0707
+    yarn_orig_len: int = 4096
 
     @property
     def row_elems(self) -> int:
@@ -72,6 +77,10 @@ SHAPES = {
                         1.0 / math.sqrt(192), 3, lengths=(131072,) * 4),
     "fp8_b32": MLAShape("fp8_b32", 32, 128, 512, 64, 128, 64, BF16, FP8, DSV2_W_STD,
                         1.0 / math.sqrt(192), 4, lengths=(8192,) * 32),
+    # the 128K context with the report's YaRN setting (section 3.1.4): s = 40, alpha = 1,
+    # beta = 32 over the 4K pre-training context, logit factor (0.0707 ln s + 1)^2
+    "yarn_b4": MLAShape("yarn_b4", 4, 128, 512, 64, 128, 64, BF16, BF16, DSV2_W_STD,
+                        1.0 / math.sqrt(192), 5, lengths=(131072,) * 4, yarn_factor=40.0),
 }
 
 

@@ -91,8 +91,18 @@ def oracle_cache(inp: S.MLAInputs, b: int):
     c_raw = inp.c_kv_raw[o0:o1].double().numpy()
     k_raw = inp.k_rope_raw[o0:o1].double().numpy()
     c, kr, _ = O.append_rows(c_raw, k_raw, np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps,
-                             theta=s.rope_theta)
+                             theta=s.rope_theta, inv_freq=oracle_inv_freq(s))
     return c, kr
+
+
+def oracle_inv_freq(s):
+    """RoPE frequencies of a workload: plain, or YaRN-scaled when s.yarn_factor > 1."""
+    return O.yarn_inv_freq(s.d_rope, s.rope_theta, s.yarn_factor, s.yarn_alpha, s.yarn_beta, s.yarn_orig_len)
+
+
+def oracle_scale(s) -> float:
+    """Softmax scale of a workload, with YaRN's logit factor when it is on."""
+    return s.scale * O.yarn_logit_factor(s.yarn_factor, s.yarn_mscale)
 
 
 def oracle_outputs(inp: S.MLAInputs, pairs: Sequence[tuple], form: str = "absorbed") -> np.ndarray:
@@ -111,5 +121,5 @@ def oracle_outputs(inp: S.MLAInputs, pairs: Sequence[tuple], form: str = "absorb
         c, kr = cache[b]
         if len(c) == 0:
             continue
-        res[n], _ = fn(q_nope[b, i], q_rope[b, i], w_uk[i], w_uv[i], c, kr, s.scale)
+        res[n], _ = fn(q_nope[b, i], q_rope[b, i], w_uk[i], w_uv[i], c, kr, oracle_scale(s))
     return res

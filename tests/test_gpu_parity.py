@@ -181,7 +181,7 @@ def test_out_of_range_page_is_flagged_not_faulted():
         M.check_device_errors()
 
 
-FULL = ["dsv2_b16", "ragged_b64", "long_b4", "fp8_b32"]
+FULL = ["dsv2_b16", "ragged_b64", "long_b4", "fp8_b32", "yarn_b4"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -48,8 +48,9 @@ def test_config_struct_layout_matches_c():
 #include <stddef.h>
 #include "mla.h"
 int main(void) {
-  printf("%zu %zu %zu %zu\n", sizeof(mla_config), offsetof(mla_config, scale),
-         offsetof(mla_config, rope_theta), offsetof(mla_config, rope_interleaved));
+  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(mla_config), offsetof(mla_config, scale),
+         offsetof(mla_config, rope_theta), offsetof(mla_config, rope_interleaved),
+         offsetof(mla_config, yarn_factor), offsetof(mla_config, yarn_orig_len));
   return 0;
 }
 '''
@@ -60,7 +61,8 @@ int main(void) {
         subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
         got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
     cc = M._CConfig
-    assert got == [ctypes.sizeof(cc), cc.scale.offset, cc.rope_theta.offset, cc.rope_interleaved.offset]
+    assert got == [ctypes.sizeof(cc), cc.scale.offset, cc.rope_theta.offset, cc.rope_interleaved.offset,
+                   cc.yarn_factor.offset, cc.yarn_orig_len.offset]
 
 
 def test_row_bytes():
@@ -90,6 +92,17 @@ def test_host_rejects_bad_config_and_arguments(lib):
     st = M._load().mla_decode(ctypes.byref(cfg), *([ctypes.c_void_p(256)] * 5), 10, None, ctypes.c_void_p(256),
                               4, 2, 129, ctypes.c_void_p(256), ctypes.c_void_p(256), 1 << 30, None)
     assert st == 1 and b"max_seq_len" in M._load().mla_last_error()
+    # YaRN on with an empty ramp (beta <= alpha) or no original context is refused
+    import dataclasses
+    for kw in (dict(yarn_beta=1.0), dict(yarn_orig_len=0)):
+        y = dataclasses.replace(M.MLAConfig.dsv2(), yarn_factor=40.0, **kw).c()
+        assert M._load().mla_cache_row_bytes(ctypes.byref(y)) == 0
+        assert b"YaRN" in M._load().mla_last_error()
+    # ... while yarn_factor <= 1 ignores the other YaRN fields
+    off = dataclasses.replace(M.MLAConfig.dsv2(), yarn_factor=1.0, yarn_beta=0.0, yarn_orig_len=0).c()
+    assert M._load().mla_cache_row_bytes(ctypes.byref(off)) == 1152
+    st = M._load().mla_rope_query(ctypes.byref(cfg), None, None, None, 2, None)
+    assert st == 1
 
 
 def test_workspace_size_grows_with_batch_and_length():
