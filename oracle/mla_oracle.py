@@ -296,6 +296,27 @@ def decode(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_seqs: Se
     return out
 
 
+def decode_multi(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_seqs: Sequence[np.ndarray],
+                 scale: float, form: str = "absorbed") -> np.ndarray:
+    """Decode of q new tokens per sequence at once (multi-token prediction drafts, DeepSeek-V3
+    summary; verified together as in speculative decoding): out [B, q, H, d_h].
+
+    q_nope [B, q, H, d_h], q_rope [B, q, H, d_r]. The cache of sequence b already holds its q new
+    tokens as its last q rows; new token k attends causally to every row up to and including
+    its own: the first L_b - (q - 1 - k) rows.
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    B, q = q_nope.shape[:2]
+    out = np.zeros(q_nope.shape)
+    for k in range(q):
+        drop = q - 1 - k
+        cs = [c[:max(0, len(c) - drop)] for c in c_seqs]
+        ks = [r[:max(0, len(r) - drop)] for r in kr_seqs]
+        out[:, k] = decode(q_nope[:, k], q_rope[:, k], w_uk, w_uv, cs, ks, scale, form)
+    return out
+
+
 def split_by_sequence(rows: np.ndarray, token_offsets: np.ndarray):
     """Cut a [sum L, ...] array into per-sequence views using prefix offsets."""
     return [rows[int(token_offsets[b]):int(token_offsets[b + 1])] for b in range(len(token_offsets) - 1)]

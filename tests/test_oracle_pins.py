@@ -393,3 +393,56 @@ def test_yarn_logit_factor_is_the_square_of_the_pages_sqrt_t():
     s, _, _, y = _yarn_facts()
     assert O.yarn_logit_factor(s, y["sqrt_t_coeff"]) == pytest.approx(O.yarn_mscale_sqrt_t(s) ** 2)
     assert O.yarn_logit_factor(1.0) == 1.0
+
+
+# ---------------------------------------------------------------------------- several new tokens per sequence
+
+def _causal_brute_force(q_nope, q_rope, w_uk, w_uv, c, kr, scale, q):
+    """Textbook causal attention of the last q positions over a cache of L rows: query k sits at
+    position L - q + k and may attend to positions j <= L - q + k (a 0 / -inf mask on the logits)."""
+    H, d_h, _ = len(w_uk), len(w_uk[0]), len(w_uk[0][0])
+    L = len(c)
+    out = np.zeros((q, H, d_h))
+    for k in range(q):
+        for i in range(H):
+            keys = [np.concatenate([np.asarray(w_uk[i]) @ c[j], kr[j]]) for j in range(L)]
+            vals = [np.asarray(w_uv[i]) @ c[j] for j in range(L)]
+            qq = np.concatenate([q_nope[k][i], q_rope[k][i]])
+            logits = [scale * float(qq @ keys[j]) if j <= L - q + k else -math.inf for j in range(L)]
+            mx = max(logits)
+            w = [math.exp(z - mx) for z in logits]
+            out[k, i] = sum(wj * vj for wj, vj in zip(w, vals)) / sum(w)
+    return out
+
+
+def test_multi_token_decode_is_causal_attention():
+    rng = np.random.default_rng(8)
+    H, d_h, d_c, d_r, q = 2, 4, 6, 2, 3
+    lens = [5, 9]
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    qn, qr = rng.standard_normal((2, q, H, d_h)), rng.standard_normal((2, q, H, d_r))
+    cs = [rng.standard_normal((L, d_c)) for L in lens]
+    ks = [rng.standard_normal((L, d_r)) for L in lens]
+    got = O.decode_multi(qn, qr, w_uk, w_uv, cs, ks, 0.41)
+    for b in range(2):
+        want = _causal_brute_force(qn[b], qr[b], w_uk, w_uv, cs[b], ks[b], 0.41, q)
+        np.testing.assert_allclose(got[b], want, rtol=1e-11, atol=1e-12)
+
+
+def test_multi_token_decode_reduces_to_decode_and_ignores_the_future():
+    rng = np.random.default_rng(9)
+    H, d_h, d_c, d_r, q, L = 3, 4, 5, 2, 4, 12
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    qn, qr = rng.standard_normal((1, q, H, d_h)), rng.standard_normal((1, q, H, d_r))
+    c, kr = rng.standard_normal((L, d_c)), rng.standard_normal((L, d_r))
+    got = O.decode_multi(qn, qr, w_uk, w_uv, [c], [kr], 0.3)
+    # the last new token sees the whole cache: plain decode
+    np.testing.assert_allclose(got[0, -1], O.decode(qn[:, -1], qr[:, -1], w_uk, w_uv, [c], [kr], 0.3)[0],
+                               rtol=1e-13, atol=1e-14)
+    # changing the rows after new token k's position leaves its output unchanged
+    c2, kr2 = c.copy(), kr.copy()
+    c2[L - 2:] += 5.0
+    kr2[L - 2:] -= 3.0
+    got2 = O.decode_multi(qn, qr, w_uk, w_uv, [c2], [kr2], 0.3)
+    np.testing.assert_array_equal(got2[0, :q - 2], got[0, :q - 2])
+    assert np.abs(got2[0, q - 2] - got[0, q - 2]).max() > 1e-3
