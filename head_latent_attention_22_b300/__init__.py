@@ -121,6 +121,8 @@ def _load():
         "mla_decode_static_scratch": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, P, P]),
         "mla_set_stage_events": (I32, [ctypes.POINTER(ctypes.c_void_p), I32]),
         "mla_rope_query": (I32, [CFG, P, P, P, I32, P]),
+        "mla_decode_multi_workspace_size": (SZ, [CFG, I32, I32, I32, I32]),
+        "mla_decode_multi": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, I32, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -257,6 +259,47 @@ def decode(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: tor
     _check(_load().mla_decode(ctypes.byref(cfg.c()), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(w_uv),
                               _ptr(pool), pool.shape[0], _ptr(block_table), _ptr(seq_lens), B, max_pages,
                               max_seq_len, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def decode_multi(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: torch.Tensor,
+                 w_uv: torch.Tensor, pool: torch.Tensor, block_table: Optional[torch.Tensor], seq_lens: torch.Tensor,
+                 max_seq_len: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 max_pages: Optional[int] = None, stream=None) -> torch.Tensor:
+    """mla_decode_multi: q_len new tokens per sequence, causal among them -> [B, q_len, H, d_head] fp32.
+
+    q_nope [B, q_len, H, d_head], q_rope [B, q_len, H, d_rope]; seq_lens counts every cached row
+    of a sequence, its q_len new tokens included."""
+    dt = cfg.io_torch_dtype
+    _need(q_nope, "q_nope", dt, 4)
+    _need(q_rope, "q_rope", dt, 4)
+    _need(w_uk, "w_uk", dt, 3)
+    _need(w_uv, "w_uv", dt, 3)
+    _need(pool, "pool", torch.uint8)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, q = q_nope.shape[:2]
+    H = cfg.n_heads
+    if q_nope.shape != (B, q, H, cfg.d_head) or q_rope.shape != (B, q, H, cfg.d_rope):
+        raise ValueError("query shapes do not match cfg")
+    if seq_lens.shape[0] != B:
+        raise ValueError("seq_lens must have one entry per sequence")
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        max_pages = block_table.shape[1]
+    if max_pages is None:
+        raise ValueError("max_pages is needed without a block table")
+    if out is None:
+        out = torch.empty((B, q, H, cfg.d_head), dtype=torch.float32, device=q_nope.device)
+    _need(out, "out", torch.float32, 4)
+    need = int(_load().mla_decode_multi_workspace_size(ctypes.byref(cfg.c()), B, q, max_pages, max_seq_len))
+    if need == 0:
+        raise MLAError(1, _load().mla_last_error().decode())
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
+    _need(workspace, "workspace", torch.uint8)
+    _check(_load().mla_decode_multi(ctypes.byref(cfg.c()), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(w_uv),
+                                    _ptr(pool), pool.shape[0], _ptr(block_table), _ptr(seq_lens), B, q, max_pages,
+                                    max_seq_len, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

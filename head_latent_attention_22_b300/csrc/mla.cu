@@ -100,6 +100,30 @@ int current_sm_count() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Virtual sequences of mla_decode_multi: v = b * q_len + k sees the first
+// seq_lens[b] - (q_len - 1 - k) rows of sequence b, through sequence b's pages.
+__global__ void expand_multi_kernel(const int32_t* seq_lens, const int32_t* block_table, int32_t* lens_v,
+                                    int32_t* table_v, int batch, int q_len, int max_pages) {
+  const int64_t n = static_cast<int64_t>(batch) * q_len * max_pages;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int p = static_cast<int>(i % max_pages);
+    const int64_t v = i / max_pages;
+    const int b = static_cast<int>(v / q_len), k = static_cast<int>(v % q_len);
+    table_v[i] = block_table ? block_table[static_cast<int64_t>(b) * max_pages + p]
+                             : static_cast<int32_t>(static_cast<int64_t>(b) * max_pages + p);
+    if (p == 0) {
+      const int L = seq_lens[b] - (q_len - 1 - k);
+      lens_v[v] = L > 0 ? L : 0;
+    }
+  }
+}
+
+size_t multi_prefix_bytes(int32_t batch, int32_t q_len, int32_t max_pages) {
+  const size_t nv = static_cast<size_t>(batch) * q_len;
+  return align_up(nv * 4, 256) + align_up(nv * static_cast<size_t>(max_pages) * 4, 256);
+}
+
 // ------------------------------------------------------------------ SIMT decode plan
 struct SimtPlan {
   int n_splits, split_tokens;
@@ -542,6 +566,43 @@ mla_status mla_rope_query(const mla_config* cfg, const void* q_rope_raw, const i
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "rope_query launch");
   return MLA_OK;
+}
+
+size_t mla_decode_multi_workspace_size(const mla_config* cfg, int32_t batch, int32_t q_len, int32_t max_pages,
+                                       int32_t max_seq_len) {
+  if (check_config(cfg) != MLA_OK || batch < 1 || q_len < 1 || max_pages < 1 || max_seq_len < 0) return 0;
+  return multi_prefix_bytes(batch, q_len, max_pages) + mla_decode_workspace_size(cfg, batch * q_len, max_seq_len);
+}
+
+mla_status mla_decode_multi(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
+                            const void* w_uv, const void* pool, int64_t num_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, int32_t batch, int32_t q_len, int32_t max_pages,
+                            int32_t max_seq_len, float* out, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (batch < 1 || q_len < 1 || max_pages < 1 || static_cast<int64_t>(batch) * q_len > (1 << 20))
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: batch=%d q_len=%d max_pages=%d", batch, q_len, max_pages);
+  if (!seq_lens || !workspace) return fail(MLA_ERR_INVALID_ARG, "seq_lens and workspace must be non-NULL");
+  if (!aligned16(workspace)) return fail(MLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  const size_t pre = multi_prefix_bytes(batch, q_len, max_pages);
+  const size_t need = mla_decode_multi_workspace_size(cfg, batch, q_len, max_pages, max_seq_len);
+  if (need == 0 || workspace_bytes < need)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+  const int nv = batch * q_len;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* lens_v = reinterpret_cast<int32_t*>(ws);
+  int32_t* table_v = reinterpret_cast<int32_t*>(ws + align_up(static_cast<size_t>(nv) * 4, 256));
+  const int64_t n = static_cast<int64_t>(nv) * max_pages;
+  const int threads = 256;
+  const int64_t want = (n + threads - 1) / threads;
+  const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+  expand_multi_kernel<<<blocks, threads, 0, as_stream(stream)>>>(seq_lens, block_table, lens_v, table_v, batch, q_len,
+                                                                  max_pages);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "decode_multi expand launch");
+  return mla_decode(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, table_v, lens_v, nv, max_pages, max_seq_len,
+                    out, ws + pre, workspace_bytes - pre, stream);
 }
 
 int32_t mla_decode_path(const mla_config* cfg) {

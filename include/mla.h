@@ -173,6 +173,29 @@ MLA_API mla_status mla_decode(const mla_config* cfg, const void* q_nope, const v
                       size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_multi - decode q_len new tokens of each sequence at once (the
+ * draft tokens of multi-token prediction, verified together; DeepSeek-V3
+ * summary, section 3). The cache already holds all q_len new tokens as the
+ * last rows of each sequence; new token k (0-based) of sequence b attends
+ * causally to the first seq_lens[b] - (q_len - 1 - k) rows (none if that is
+ * not positive):
+ *   q_nope [batch, q_len, n_heads, d_head], q_rope [batch, q_len, n_heads, d_rope]
+ *   out    [batch, q_len, n_heads, d_head] fp32
+ * Other arguments as mla_decode; the workspace is
+ * mla_decode_multi_workspace_size(cfg, batch, q_len, max_pages, max_seq_len)
+ * bytes (0 for invalid arguments).
+ * Each new token is decoded as a sequence of its own over the pages of its
+ * sequence, so the q_len of them read the same pages while those are in L2.
+ */
+MLA_API size_t mla_decode_multi_workspace_size(const mla_config* cfg, int32_t batch, int32_t q_len,
+                                               int32_t max_pages, int32_t max_seq_len);
+MLA_API mla_status mla_decode_multi(const mla_config* cfg, const void* q_nope, const void* q_rope,
+                                    const void* w_uk, const void* w_uv, const void* pool, int64_t num_pages,
+                                    const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                                    int32_t q_len, int32_t max_pages, int32_t max_seq_len, float* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_static_scratch - mla_decode that allocates nothing and takes no
  * workspace argument. The paper has no counterpart to this call; it exists
  * for callers of this library that cannot allocate device memory at the
