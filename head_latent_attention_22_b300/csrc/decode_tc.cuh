@@ -973,9 +973,11 @@ __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
     bool use[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
+      // the loads do not wait for the share check: a slot of an empty share (which wrote
+      // no partial) is read and then ignored, so all loads are one round trip
       const int c = cb + u;
-      use[u] = c <= c1 && start[c] < start[c + 1];   // an empty share wrote no partial
-      if (use[u]) {
+      use[u] = c <= c1 && start[c] < start[c + 1];
+      if (c <= c1) {
         ml[u] = ml_all[static_cast<int64_t>(b + c) * kH + h];
         o[u] = *reinterpret_cast<const float4*>(a.part_o + parto_index(b + c, chunk, h));
       }
