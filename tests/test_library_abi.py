@@ -109,3 +109,29 @@ def test_workspace_size_grows_with_batch_and_length():
     cfg = M.MLAConfig.dsv2()
     a = M.workspace_size(cfg, 4, 4096)
     assert a > 0 and M.workspace_size(cfg, 8, 4096) > a and M.workspace_size(cfg, 4, 131072) >= a
+
+
+def test_host_rejects_bad_multi_token_and_rope_query_arguments(lib):
+    L = M._load()
+    cfg = M.MLAConfig.dsv2().c()
+    P = ctypes.c_void_p
+    # workspace size: invalid sizes give 0, valid ones grow with q_len
+    assert L.mla_decode_multi_workspace_size(ctypes.byref(cfg), 4, 0, 64, 4096) == 0
+    assert L.mla_decode_multi_workspace_size(ctypes.byref(cfg), 0, 2, 64, 4096) == 0
+    w1 = L.mla_decode_multi_workspace_size(ctypes.byref(cfg), 4, 1, 64, 4096)
+    w3 = L.mla_decode_multi_workspace_size(ctypes.byref(cfg), 4, 3, 64, 4096)
+    assert 0 < w1 < w3
+    # q_len 0, a missing workspace and a too-small workspace are refused before any launch
+    st = L.mla_decode_multi(ctypes.byref(cfg), *([P(256)] * 5), 10, None, P(256), 4, 0, 64, 4096, P(256), P(256),
+                            1 << 30, None)
+    assert st == 1
+    st = L.mla_decode_multi(ctypes.byref(cfg), *([P(256)] * 5), 10, None, P(256), 4, 2, 64, 4096, P(256), None,
+                            1 << 30, None)
+    assert st == 1 and b"non-NULL" in L.mla_last_error()
+    st = L.mla_decode_multi(ctypes.byref(cfg), *([P(256)] * 5), 10, None, P(256), 4, 2, 64, 4096, P(256), P(256),
+                            16, None)
+    assert st == 1 and b"too small" in L.mla_last_error()
+    # rope_query: negative batch and NULL pointers are refused; an empty batch is a no-op
+    assert L.mla_rope_query(ctypes.byref(cfg), P(256), P(256), P(256), -1, None) == 1
+    assert L.mla_rope_query(ctypes.byref(cfg), None, P(256), P(256), 2, None) == 1
+    assert L.mla_rope_query(ctypes.byref(cfg), None, None, None, 0, None) == 0
