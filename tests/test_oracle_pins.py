@@ -446,3 +446,21 @@ def test_multi_token_decode_reduces_to_decode_and_ignores_the_future():
     got2 = O.decode_multi(qn, qr, w_uk, w_uv, [c2], [kr2], 0.3)
     np.testing.assert_array_equal(got2[0, :q - 2], got[0, :q - 2])
     assert np.abs(got2[0, q - 2] - got[0, q - 2]).max() > 1e-3
+
+
+def test_prefill_is_the_multi_token_decode_over_every_position():
+    # prefill (every prompt token a query, causal) is the multi-token decode with q = L; its
+    # explicit form (per-head K and V materialised, as prefill kernels compute it) agrees with
+    # the absorbed one
+    rng = np.random.default_rng(10)
+    H, d_h, d_c, d_r, L = 2, 4, 6, 2, 7
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    qn, qr = rng.standard_normal((1, L, H, d_h)), rng.standard_normal((1, L, H, d_r))
+    c, kr = rng.standard_normal((L, d_c)), rng.standard_normal((L, d_r))
+    a = O.decode_multi(qn, qr, w_uk, w_uv, [c], [kr], 0.5, form="absorbed")
+    e = O.decode_multi(qn, qr, w_uk, w_uv, [c], [kr], 0.5, form="explicit")
+    np.testing.assert_allclose(a, e, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(a[0], _causal_brute_force(qn[0], qr[0], w_uk, w_uv, c, kr, 0.5, L), rtol=1e-11,
+                               atol=1e-12)
+    # the first token attends only to itself: its value
+    np.testing.assert_allclose(a[0, 0], np.einsum("hdk,k->hd", w_uv, c[0]), rtol=1e-12, atol=1e-13)
