@@ -6,11 +6,11 @@
 // quantised KV cache).
 //
 // Four kernels per decode:
-//   absorb  : Q_lat[b,i,0:512] = W_UK[i]^T q_nope[b,i] (one CTA per head, the
-//             whole 128 KB weight slice in flight at once, M = 4 x 128 latent
-//             rows, N = batch), q_rope copied to Q_lat[b,i,512:576]; one
-//             extra CTA clamps the lengths and writes the per-sequence tile
-//             prefix sums the other two kernels share.
+//   absorb  : Q_lat[b,i,0:512] = W_UK[i]^T q_nope[b,i] (two CTAs per head, each
+//             with its 64 KB half of the weight slice in flight at once, M = 2 x
+//             128 latent rows, N = batch), q_rope copied to Q_lat[b,i,512:576];
+//             one extra CTA clamps the lengths and writes the plan the other
+//             kernels share (tile prefix sums, cluster shares).
 //   attend  : persistent clusters of two CTAs; cluster c takes an equal share
 //             of all 64-token tiles of all sequences, cut at sequence ends
 //             into segments. In a pair, CTA0 owns latent columns 0..255 plus
