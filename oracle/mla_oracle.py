@@ -317,11 +317,6 @@ def decode_multi(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_se
     return out
 
 
-def split_by_sequence(rows: np.ndarray, token_offsets: np.ndarray):
-    """Cut a [sum L, ...] array into per-sequence views using prefix offsets."""
-    return [rows[int(token_offsets[b]):int(token_offsets[b + 1])] for b in range(len(token_offsets) - 1)]
-
-
 # ----------------------------------------------------------------------------
 # closed forms from the pages
 
