@@ -389,10 +389,42 @@ def test_yarn_rope_keeps_norm_and_relative_position_property():
         assert np.linalg.norm(qm) == pytest.approx(np.linalg.norm(q))
 
 
-def test_yarn_logit_factor_is_the_square_of_the_pages_sqrt_t():
-    s, _, _, y = _yarn_facts()
-    assert O.yarn_logit_factor(s, y["sqrt_t_coeff"]) == pytest.approx(O.yarn_mscale_sqrt_t(s) ** 2)
+def test_yarn_logit_factor_is_what_scaling_query_and_key_by_sqrt_t_does():
+    # Section 3.1.4 gives sqrt(t) = 0.0707 ln s + 1 as a factor on the query and on the key (as in
+    # YaRN). Scale a query and a key each by that factor, rotate both with the YaRN frequencies, and
+    # their dot product must be the unscaled one times yarn_logit_factor(s): a factor that used
+    # sqrt(t) instead of t, or squared it twice, fails here.
+    s, a, b, y = _yarn_facts()
+    rng = np.random.default_rng(11)
+    f = O.yarn_inv_freq(64, 1e4, s, a, b, 4096)
+    sq = O.yarn_mscale_sqrt_t(s)
+    for m, n in [(130000, 1234), (77, 76), (4095, 0)]:
+        q, k = rng.standard_normal(64), rng.standard_normal(64)
+        plain = O.rope(q, m, 1e4, inv_freq=f) @ O.rope(k, n, 1e4, inv_freq=f)
+        scaled = O.rope(sq * q, m, 1e4, inv_freq=f) @ O.rope(sq * k, n, 1e4, inv_freq=f)
+        assert scaled == pytest.approx(O.yarn_logit_factor(s, y["sqrt_t_coeff"]) * plain, rel=1e-12)
     assert O.yarn_logit_factor(1.0) == 1.0
+
+
+def test_yarn_logit_factor_on_the_scale_equals_scaled_explicit_queries_and_keys():
+    # The decode applies t as a factor on the softmax scale of the absorbed form. The same result
+    # must come from the explicit form of sections 2.1.2-2.1.3 whose whole query [q_C ; q_R] and
+    # whole key [W_UK c ; k_R] are each multiplied by sqrt(t) (the values W_UV c are not).
+    s, _, _, _ = _yarn_facts()
+    rng = np.random.default_rng(12)
+    d_h, d_c, d_r, L = 16, 32, 8, 37
+    qn, qr = rng.standard_normal(d_h), rng.standard_normal(d_r)
+    w_uk, w_uv = 0.3 * rng.standard_normal((d_h, d_c)), 0.3 * rng.standard_normal((d_h, d_c))
+    c, kr = rng.standard_normal((L, d_c)), rng.standard_normal((L, d_r))
+    scale = 1 / math.sqrt(d_h + d_r)
+    sq = O.yarn_mscale_sqrt_t(s)
+    want, p_want = O.head_explicit(sq * qn, sq * qr, sq * w_uk, w_uv, c, sq * kr, scale)
+    got, p_got = O.head_absorbed(qn, qr, w_uk, w_uv, c, kr, scale * O.yarn_logit_factor(s))
+    np.testing.assert_allclose(p_got, p_want, rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(got, want, rtol=1e-10, atol=1e-12)
+    # and the factor is not a no-op here: without it the weights differ
+    _, p_plain = O.head_absorbed(qn, qr, w_uk, w_uv, c, kr, scale)
+    assert np.max(np.abs(p_plain - p_want)) > 1e-3
 
 
 # ---------------------------------------------------------------------------- several new tokens per sequence
