@@ -14,7 +14,6 @@ from __future__ import annotations
 
 import ctypes
 import dataclasses
-import math
 import os
 from typing import Optional
 
@@ -62,7 +61,7 @@ class MLAConfig:
     page_size: int = 64
     io_dtype: int = BF16
     cache_dtype: int = BF16
-    scale: float = 0.0          # 0 => 1/sqrt(d_head + d_rope)
+    scale: float = 0.0          # <= 0: the library uses 1/sqrt(d_head + d_rope)
     eps: float = 1e-6
     rope_theta: float = 10000.0
     rope_interleaved: bool = True
@@ -87,9 +86,8 @@ class MLAConfig:
                          int(shape.yarn_orig_len))
 
     def c(self) -> _CConfig:
-        scale = self.scale if self.scale else 1.0 / math.sqrt(self.d_head + self.d_rope)
         return _CConfig(self.n_heads, self.d_c, self.d_rope, self.d_head, self.page_size, self.io_dtype,
-                        self.cache_dtype, scale, self.eps, self.rope_theta, int(self.rope_interleaved),
+                        self.cache_dtype, self.scale, self.eps, self.rope_theta, int(self.rope_interleaved),
                         self.yarn_factor, self.yarn_alpha, self.yarn_beta, self.yarn_mscale, self.yarn_orig_len)
 
     @property

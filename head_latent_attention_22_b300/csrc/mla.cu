@@ -82,11 +82,15 @@ RopeFreq rope_freq_of(const mla_config* c) {
   return r;
 }
 
-// Softmax scale of the decode: cfg->scale, times YaRN's logit factor (mscale ln s + 1)^2.
+// Softmax scale of the decode: cfg->scale (1/sqrt(d_head + d_rope) when it is
+// not positive: the width of the full key [k_C ; k_R]), times YaRN's logit
+// factor (mscale ln s + 1)^2.
 float softmax_scale(const mla_config* c) {
-  if (!yarn_on(c)) return c->scale;
+  const double base = c->scale > 0.f ? static_cast<double>(c->scale)
+                                     : 1.0 / std::sqrt(static_cast<double>(c->d_head + c->d_rope));
+  if (!yarn_on(c)) return static_cast<float>(base);
   const double m = static_cast<double>(c->yarn_mscale) * std::log(static_cast<double>(c->yarn_factor)) + 1.0;
-  return static_cast<float>(static_cast<double>(c->scale) * m * m);
+  return static_cast<float>(base * m * m);
 }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -216,7 +220,7 @@ bool tc_supported(const mla_config* c) {
   return c->n_heads == tcd::kH && c->d_c == tcd::kDc && c->d_rope == tcd::kDr && c->d_head == tcd::kDh &&
          c->io_dtype == MLA_DTYPE_BF16 &&
          (c->cache_dtype == MLA_DTYPE_BF16 || c->cache_dtype == MLA_DTYPE_FP8_E4M3_B128) &&
-         c->page_size % tcd::kTile == 0 && c->scale > 0.f;
+         c->page_size % tcd::kTile == 0;
 }
 
 // Clusters the workspace is sized for; a launch never uses more.
@@ -458,26 +462,16 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
 // ------------------------------------------------------------------ fixed scratch
 // Scratch of mla_decode_static_scratch: one array per device, for callers
 // that cannot allocate. Host code must not use the symbol as an address; the
-// device address comes from cudaGetSymbolAddress, once per device.
+// device address comes from cudaGetSymbolAddress. It is looked up on every
+// call (the lookup allocates nothing), so a module reloaded after a device
+// reset is never used through a stale address.
 static __device__ __align__(256) unsigned char g_static_scratch[MLA_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_scratch_mu;
-void* g_static_scratch_addr[kMaxDevices] = {};
-
 mla_status static_scratch_address(void** addr) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device %d beyond %d devices", dev, kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-  if (!g_static_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_static_scratch_addr[dev] = p;
-  }
-  *addr = g_static_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  *addr = p;
   return MLA_OK;
 }
 

@@ -70,7 +70,8 @@ typedef struct {
   int32_t page_size;        /* tokens per cache page */
   int32_t io_dtype;         /* mla_dtype of queries, weights, raw latents/keys: BF16 or FP32 */
   int32_t cache_dtype;      /* mla_dtype of the pool rows */
-  float scale;              /* softmax scale applied to q.k (e.g. 1/sqrt(d_h + d_rope)) */
+  float scale;              /* softmax scale applied to q.k; <= 0 selects 1/sqrt(d_head + d_rope), the
+                               width of the full key [k_C ; k_R] (report sections 2.1.1, 2.1.3) */
   float eps;                /* RMSNorm epsilon */
   float rope_theta;         /* RoPE base; pair m turns by pos * theta^(-2m/d_rope) */
   int32_t rope_interleaved; /* 1: pairs (2m, 2m+1) (RoFormer); 0: pairs (m, m + d_rope/2) */
@@ -212,9 +213,12 @@ MLA_API mla_status mla_decode_multi(const mla_config* cfg, const void* q_nope, c
  * (mla_decode_workspace_size() > MLA_STATIC_SCRATCH_BYTES) is refused with
  * MLA_ERR_INVALID_ARG before anything is launched; nothing is allocated.
  *
- * The first call on a device (with that device current) looks up the
- * array's device address with cudaGetSymbolAddress; make that first call
- * before any stream capture. All calls on a device share the one array, so
+ * Every call looks up the array's device address on the current device
+ * with cudaGetSymbolAddress (which allocates nothing); the first call on a
+ * device also loads the library's device code there, so make that first call
+ * before any stream capture. For the DeepSeek-V2 shape on the tensor-core
+ * path (128 heads, d_c 512, d_rope 64, d_head 128) the array holds the
+ * scratch of a batch of at most 25 sequences, whatever their lengths. All calls on a device share the one array, so
  * two calls whose kernels overlap on the GPU (different streams, or threads
  * without ordering) race on it and both results are undefined; serialise
  * them. The array keeps the last call's contents; the decode writes every

@@ -135,3 +135,29 @@ def test_host_rejects_bad_multi_token_and_rope_query_arguments(lib):
     assert L.mla_rope_query(ctypes.byref(cfg), P(256), P(256), P(256), -1, None) == 1
     assert L.mla_rope_query(ctypes.byref(cfg), None, P(256), P(256), 2, None) == 1
     assert L.mla_rope_query(ctypes.byref(cfg), None, None, None, 0, None) == 0
+
+
+def test_default_scale_is_left_to_the_library(lib):
+    # scale <= 0 asks the library for 1/sqrt(d_head + d_rope); the binding passes it through untouched
+    cfg = M.MLAConfig.dsv2()
+    assert cfg.scale == 0.0 and cfg.c().scale == 0.0
+    assert M.decode_path(cfg) == 1   # the tensor-core path accepts the default
+
+
+def test_static_scratch_batch_limit_matches_the_header(lib):
+    L = M._load()
+    P = ctypes.c_void_p
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    limit = int(re.search(r"MLA_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << 20\)", text).group(1)) << 20
+    n_doc = int(re.search(r"batch of at most (\d+) sequences", text).group(1))
+    cfg = M.MLAConfig.dsv2()
+    assert M.workspace_size(cfg, n_doc, 131072) <= limit < M.workspace_size(cfg, n_doc + 1, 131072)
+    c = cfg.c()
+    # one past the limit: refused for its size, before anything is looked up or launched
+    st = L.mla_decode_static_scratch(ctypes.byref(c), *([P(256)] * 5), 10, None, P(256), n_doc + 1, 2, 4096,
+                                     P(256), None)
+    assert st == 1 and b"bytes of scratch" in L.mla_last_error()
+    # at the limit the size passes; the call then stops on the (deliberately) short page table
+    st = L.mla_decode_static_scratch(ctypes.byref(c), *([P(256)] * 5), 10, None, P(256), n_doc, 2, 4096,
+                                     P(256), None)
+    assert st != 0 and b"bytes of scratch" not in L.mla_last_error()
