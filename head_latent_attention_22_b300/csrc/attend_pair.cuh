@@ -1,0 +1,463 @@
+// Attend step of the tensor-core MLA decode on a CTA pair whose MMAs are
+// pair MMAs (tcgen05 cta_group::2), for a bf16 latent cache (DeepSeek-V2
+// report, section 2.1.2: scores and values both read the shared latent;
+// section 2.1.3: the decoupled rope key adds to the scores).
+//
+// Why this shape. The output accumulator O_lat of 128 heads x 512 latent
+// values in fp32 fills one SM's tensor memory, so two SMs share every tile.
+// Splitting the work so that each SM owns 64 heads end to end needs no
+// software exchange between them: the pair MMA moves operand halves between
+// the two SMs itself. Each CTA keeps half of every cache tile (its 256 latent
+// columns and 32 of the 64 rope columns) and the queries of its 64 heads.
+//
+//   scores  S = Q K^T: one pair MMA per 16-wide step of the contraction, M = 256
+//           rows (per CTA: 64 heads x the two halves of the contraction), N = 128
+//           (64 tokens x the two halves), K = 288. Of each CTA's 128 x 128 result
+//           only the blocks (head, half A) x (token, half A) and (head, half B) x
+//           (token, half B) are used; their sum is the score. This costs twice
+//           the MACs of the score but runs 18 full-rate MMAs per tile, where a
+//           64-column MMA would be held up by the tensor pipe's fixed cost per
+//           instruction.
+//   softmax each CTA only for its 64 heads (8 warps, 16 scores per thread).
+//   PV      O += P V: pair MMA, M = 128 (64 heads per CTA), N = 256 latent
+//           columns per MMA (128 from each CTA's half), K = 64 tokens.
+//
+// Tensor memory (512 columns): two score buffers of 128 columns, then O as two
+// 128-column halves (the pair-MMA layout puts row m of a CTA's 64 in lanes m and
+// m + 64, each with one half of the N columns).
+#pragma once
+
+#include "common.cuh"
+#include "decode_tc.cuh"
+#include "tc.cuh"
+
+namespace mla {
+namespace tcd {
+
+constexpr int kPrStages = 3;                        // cache tile ring depth
+constexpr int kPrBox = kTile * 128;                 // one TMA box: 64 rows x 64 bf16 = 8 KB
+constexpr int kPrStageBytes = 5 * kPrBox;           // 4 latent boxes + 1 rope box per CTA
+constexpr int kPrQBox = 128 * 128;                  // 128 rows x 64 bf16 = 16 KB
+constexpr int kPrQBytes = 5 * kPrQBox;              // queries of 64 heads, both contraction halves
+constexpr int kPrPBytes = 64 * 128;                 // P: 64 heads x 64 tokens bf16
+constexpr int kPrSoftmaxWarps = 8;
+constexpr int kPrThreads = 32 * (4 + kPrSoftmaxWarps);   // TMA, MMA, forwarder, query loader, softmax
+constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
+constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
+constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
+
+struct PairSmem {
+  uint64_t full[kPrStages];    // this CTA's half of a tile landed (TMA)
+  uint64_t empty[kPrStages];   // the PV of the tile in the slot completed (pair commit)
+  uint64_t ready[kPrStages];   // even CTA: both halves of a tile landed (one arrival per CTA)
+  uint64_t qfull, qfree, qready;
+  uint64_t s_full[2];          // scores of a tile are in TMEM (pair commit)
+  uint64_t s_free[2];          // even CTA: all softmax warps of both CTAs read them
+  uint64_t p_full;             // even CTA: P written, O rescaled, tail rows cleared, in both CTAs
+  uint64_t o_done;             // a PV completed (pair commit)
+  uint64_t o_free;             // even CTA: both CTAs read O at a segment end
+  uint64_t drain;
+  float red_max[2][2][64];     // [tile parity][token half][head] row maxima of the two warps of a head
+  float alpha[2][64];          // [tile parity][head] rescale factor of O (1 when unchanged)
+  float red_l[2][64];          // [token half][head] row sums at a segment end
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+constexpr size_t kPrSmem = 1024 + kPrQBytes + static_cast<size_t>(kPrStages) * kPrStageBytes + kPrPBytes +
+                           sizeof(PairSmem);
+
+__device__ __forceinline__ bool pr_aborted(const PairSmem* s) {
+  return *reinterpret_cast<const volatile int32_t*>(&s->abort_flag) != 0;
+}
+__device__ __forceinline__ void pr_set_abort(PairSmem* s) {
+  *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1;
+}
+
+// map_lat: the bf16 pool [rows, 576], boxes of 64 rows x 64 columns, 128-byte swizzle.
+// map_q:   Q_lat row-major [B * 128 heads, 576] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
+    attend_pair_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_q,
+                       AttendArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = sm;                                   // 5 boxes [128 rows x 64]
+  uint8_t* stages = sm + kPrQBytes;                   // kPrStages x 5 boxes [64 tokens x 64]
+  uint8_t* sP = stages + kPrStages * kPrStageBytes;   // [64 heads x 64 tokens]
+  PairSmem* S = reinterpret_cast<PairSmem*>(sP + kPrPBytes);
+
+  const uint32_t rank = tc::cluster_ctarank();
+  const uint32_t cl = tc::cluster_id_x(), ncl = tc::n_clusters_x();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPrStages; ++s) {
+      tc::mbar_init(&S->full[s], 1);
+      tc::mbar_init(&S->empty[s], 1);
+      tc::mbar_init(&S->ready[s], 2);
+    }
+    tc::mbar_init(&S->qfull, 1);
+    tc::mbar_init(&S->qfree, 1);
+    tc::mbar_init(&S->qready, 2);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&S->s_full[b], 1);
+      tc::mbar_init(&S->s_free[b], 2 * kPrSoftmaxWarps);
+    }
+    tc::mbar_init(&S->p_full, 2 * kPrSoftmaxWarps);
+    tc::mbar_init(&S->o_done, 1);
+    tc::mbar_init(&S->o_free, 2 * kPrSoftmaxWarps);
+    tc::mbar_init(&S->drain, 1);
+    S->abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_map(&map_lat);
+    tc::tma_prefetch_map(&map_q);
+  }
+  if (warp == 1) tc::tmem_alloc_pair<512>(&S->tmem_base);
+  tc::tc_fence_before();
+  tc::cluster_sync();
+  tc::tc_fence_after();
+  const uint32_t tm = S->tmem_base;
+  // everything below reads what the absorb kernel wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int32_t* cum = a.plan.cum;
+  const uint32_t n_share = static_cast<uint32_t>(a.plan.share_start[cl + 1] - a.plan.share_start[cl]);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- cache tiles (both CTAs: own half)
+    const uint64_t policy = tc::policy_evict_first();
+    SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
+    int b, j0, j1;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+      for (int jc = j0; jc < j1 && ok; jc += 32) {
+        int32_t y_l = 0;
+        const int jl = jc + lane;
+        if (jl < j1) {
+          const int64_t tok = static_cast<int64_t>(jl) * kTile;
+          const int pg = static_cast<int>(tok / a.page_size);
+          int64_t page = -1;
+          if (pg < a.max_pages)
+            page = a.block_table ? a.block_table[static_cast<int64_t>(b) * a.max_pages + pg]
+                                 : static_cast<int64_t>(b) * a.max_pages + pg;
+          if (page < 0 || page >= a.num_pages) {
+            flag_error(ERR_BIT_BOUNDS);
+            y_l = -2 * kTile;  // entirely outside the pool: the copy fills zeros
+          } else {
+            y_l = static_cast<int32_t>(page * a.page_size + tok % a.page_size);
+          }
+        }
+        const int n = min(32, j1 - jc);
+        for (int u = 0; u < n; ++u) {
+          const int32_t y = __shfl_sync(0xffffffffu, y_l, u);
+          if (lane == 0 && ok) {
+            const int st = it % kPrStages;
+            if (it >= kPrStages) ok = tc::mbar_wait(&S->empty[st], ((it / kPrStages) - 1) & 1);
+            if (ok && pr_aborted(S)) ok = false;
+            if (ok) {
+              uint8_t* dst = stages + st * kPrStageBytes;
+              tc::mbar_arrive_expect_tx(&S->full[st], kPrStageBytes);
+              for (int k = 0; k < 4; ++k)
+                tc::tma_load_2d_hint(dst + k * kPrBox, &map_lat, static_cast<int>(rank) * 256 + 64 * k, y,
+                                     &S->full[st], policy);
+              // rope columns 32 rank .. 32 rank + 31 land in box columns 0..31 (the odd CTA's
+              // box reaches past the row end: those columns are filled with zeros)
+              tc::tma_load_2d_hint(dst + 4 * kPrBox, &map_lat, kDc + 32 * static_cast<int>(rank), y, &S->full[st],
+                                   policy);
+              ++it;
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+        }
+      }
+    }
+    it = __shfl_sync(0xffffffffu, it, 0);
+    if (lane == 0) {
+      if (!ok) pr_set_abort(S);
+      const uint32_t first = it > kPrStages ? it - kPrStages : 0;
+      for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kPrStages], (q / kPrStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- pair MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc_s = tc::idesc_bf16_f32(256, 128, 0, 0);
+      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+      const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);       // K-major Q, 128 rows
+      const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), 16, 1024);   // K-major tile, 64 rows
+      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), kPrBox, 1024);   // MN-major V
+      const uint64_t pdesc0 = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);       // K-major P, 64 rows
+      SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
+      int b, j0, j1;
+      uint32_t it = 0, seg = 0;
+      bool ok = true;
+      // the PV of the previous tile goes out after the scores of the next one, so the
+      // softmax of a tile overlaps the score MMAs of the following tile
+      bool have_pv = false;
+      uint32_t pv_it = 0, pv_seg = 0;
+      bool pv_first = false;
+      auto issue_pv = [&]() -> bool {
+        if (!tc::mbar_wait_cl(&S->p_full, pv_it & 1)) return false;
+        if (pv_first && pv_seg > 0 && !tc::mbar_wait_cl(&S->o_free, (pv_seg - 1) & 1)) return false;
+        if (pr_aborted(S)) return false;
+        tc::tc_fence_after();
+        const uint32_t st = pv_it % kPrStages;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = pdesc0 + static_cast<uint64_t>((kk * 32) >> 4);
+            const uint64_t bd = vdesc0 + static_cast<uint64_t>((st * kPrStageBytes + 2 * h * kPrBox + kk * 2048) >> 4);
+            tc::mma_ss_pair(tm + kPrTmO + 128 * h, ad, bd, idesc_o, (pv_first && kk == 0) ? 0u : 1u);
+          }
+        }
+        tc::mma_commit_pair(&S->o_done);
+        tc::mma_commit_pair(&S->empty[st]);
+        return true;
+      };
+      while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+        ok = tc::mbar_wait_cl(&S->qready, seg & 1);
+        for (int j = j0; j < j1 && ok; ++j, ++it) {
+          const uint32_t st = it % kPrStages;
+          ok = tc::mbar_wait_cl(&S->ready[st], (it / kPrStages) & 1);
+          if (ok && it >= 2) ok = tc::mbar_wait_cl(&S->s_free[it & 1], ((it - 2) >> 1) & 1);
+          if (!ok || pr_aborted(S)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t d = tm + kPrTmS + 128 * (it & 1);
+#pragma unroll
+          for (int k = 0; k < kPrKSteps; ++k) {
+            const int box = k < 16 ? (k >> 2) : 4;
+            const int off = (k < 16 ? (k & 3) : (k - 16)) * 32;
+            const uint64_t ad = qdesc0 + static_cast<uint64_t>((box * kPrQBox + off) >> 4);
+            const uint64_t bd = kdesc0 + static_cast<uint64_t>((st * kPrStageBytes + box * kPrBox + off) >> 4);
+            tc::mma_ss_pair(d, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          }
+          tc::mma_commit_pair(&S->s_full[it & 1]);
+          if (j == j1 - 1) tc::mma_commit_pair(&S->qfree);   // the queries may be replaced
+          if (have_pv && !issue_pv()) { ok = false; break; }
+          have_pv = true;
+          pv_it = it;
+          pv_seg = seg;
+          pv_first = j == j0;
+        }
+        ++seg;
+      }
+      if (ok && have_pv) ok = issue_pv();
+      if (!ok) pr_set_abort(S);
+      // every MMA issued so far must complete before TMEM is released
+      tc::mma_commit_pair(&S->drain);
+      tc::mbar_wait(&S->drain, 0);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- tile forwarder (both CTAs)
+    // tells the even CTA's MMA issuer that this CTA's half of a tile has landed
+    if (lane == 0) {
+      const uint32_t ready0 = tc::map_peer(&S->ready[0], 0);
+      for (uint32_t it = 0; it < n_share; ++it) {
+        const uint32_t st = it % kPrStages;
+        if (!tc::mbar_wait(&S->full[st], (it / kPrStages) & 1) || pr_aborted(S)) {
+          pr_set_abort(S);
+          break;
+        }
+        tc::mbar_arrive_cluster(ready0 + 8u * st);
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- queries of this CTA's 64 heads
+    // row r = 32 q + i of each box: head 16 q + (i mod 16), contraction half i / 16 (half A: latent
+    // 0..255 and rope 0..31, the even CTA's columns; half B: latent 256..511 and rope 32..63)
+    if (lane == 0) {
+      const uint32_t qready = tc::map_peer(&S->qready, 0);
+      SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
+      int b, j0, j1;
+      uint32_t seg = 0;
+      bool ok = true;
+      while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+        if (seg > 0) ok = tc::mbar_wait(&S->qfree, (seg - 1) & 1);
+        if (!ok || pr_aborted(S)) { ok = false; break; }
+        tc::mbar_arrive_expect_tx(&S->qfull, kPrQBytes);
+        const int row0 = b * kH + 64 * static_cast<int>(rank);
+        for (int q = 0; q < 4; ++q)
+          for (int half = 0; half < 2; ++half)
+            for (int k = 0; k < 5; ++k)
+              tc::tma_load_2d(sQ + k * kPrQBox + (32 * q + 16 * half) * 128, &map_q,
+                              k < 4 ? 256 * half + 64 * k : kDc + 32 * half, row0 + 16 * q, &S->qfull);
+        ok = tc::mbar_wait(&S->qfull, seg & 1);
+        if (!ok) break;
+        tc::mbar_arrive_cluster(qready);
+        ++seg;
+      }
+      if (!ok) pr_set_abort(S);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax + segment epilogue
+    const int q = warp & 3, w2 = (warp - 4) >> 2;     // lane quarter; token half (32 w2 .. 32 w2 + 31)
+    const int hl = 16 * q + (lane & 15);              // this CTA's head whose scores this thread finishes
+    const int part = lane >> 4;                       // which 16 of the warp's 32 tokens it finishes
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t s_free0 = tc::map_peer(&S->s_free[0], 0);
+    const uint32_t p_full = tc::map_peer(&S->p_full, 0);
+    const uint32_t o_free = tc::map_peer(&S->o_free, 0);
+    const float sl = a.scale_log2;
+    // O lanes this thread reads or rescales: lane 32 q + lane holds head (32 q + lane) mod 64 of this
+    // CTA, latent columns (lane >= 64 ? 256 : 0) + 128 w2 .. + 127 in TMEM columns kPrTmO + 128 w2 ..
+    const int o_head = (32 * q + lane) & 63;
+    const int o_lat0 = (32 * q + lane >= 64 ? 256 : 0) + 128 * w2;
+    const uint32_t t_o = tm + lane_base + kPrTmO + 128 * w2;
+
+    // Every barrier below is passed by all softmax threads the same number of times: a wait
+    // that runs out only marks the tile bad, and the threads leave together after a vote.
+    SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
+    int b, j0, j1;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+      const int L = a.plan.lens[b];
+      const int slot = b + static_cast<int>(cl);
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = j0; j < j1 && ok; ++j, ++it) {
+        const int valid = min(kTile, L - j * kTile);
+        bool good = tc::mbar_wait(&S->s_full[it & 1], (it >> 1) & 1) && !pr_aborted(S);
+        tc::tc_fence_after();
+        float s[16];
+        {
+          uint32_t ra[32], rb[32];
+          const uint32_t t_s = tm + lane_base + kPrTmS + 128 * (it & 1) + 32 * w2;
+          tc::tmem_ld32(t_s, ra);        // lanes of half A: this head's half-A scores of 32 tokens
+          tc::tmem_ld32(t_s + 64, rb);   // lanes of half B: its half-B scores of the same tokens
+          tc::tmem_ld_wait();
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive_cluster(s_free0 + 8u * (it & 1));
+          // the two halves of a head sit in lanes i and i + 16 of the warp: swap the 16 tokens
+          // each of them finishes
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const uint32_t send = part ? rb[jj] : ra[16 + jj];
+            const float r = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+            s[jj] = __uint_as_float(part ? rb[16 + jj] : ra[jj]) + r;
+          }
+        }
+        const int vt = valid - (32 * w2 + 16 * part);   // valid tokens among this thread's 16
+        if (vt < 16) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (jj >= vt) s[jj] = -INFINITY;
+        }
+        float mx;
+        {
+          float t4[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) t4[c] = fmaxf(fmaxf(s[c], s[c + 4]), fmaxf(s[c + 8], s[c + 12]));
+          mx = fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3]));
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        S->red_max[it & 1][w2][hl] = mx;
+        tc::named_sync(1 + q, 64);   // the two warps holding this quarter's heads
+        mx = fmaxf(S->red_max[it & 1][0][hl], S->red_max[it & 1][1][hl]) * sl;
+        bool resc = false;
+        float alpha = 1.f;
+        if (m_used == -INFINITY) {
+          m_used = mx;
+        } else if (mx > m_used + kRescaleThreshold) {
+          alpha = tc::ex2_approx(m_used - mx);
+          l *= alpha;
+          m_used = mx;
+          resc = true;
+        }
+        const float neg_m = -m_used;
+        uint32_t p[8];
+        float ps[2] = {0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t w = tc::pack_bf16(tc::ex2_approx(fmaf(s[2 * c], sl, neg_m)),
+                                           tc::ex2_approx(fmaf(s[2 * c + 1], sl, neg_m)));
+          p[c] = w;
+          ps[c & 1] += bf_lo(w) + bf_hi(w);
+        }
+        l += ps[0] + ps[1];
+        if (lane < 16) S->alpha[it & 1][hl] = alpha;
+        // the PV of the previous tile must be done: P and O are ours
+        if (it > 0) good = tc::mbar_wait(&S->o_done, (it - 1) & 1) && good;
+        tc::tc_fence_after();
+        if (tc::named_sync_or(5, 32 * kPrSoftmaxWarps, resc)) {
+          // a head's O rows are lanes h and h + 64: the threads on those lanes rescale them
+          const float f = S->alpha[it & 1][o_head];
+          if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+              uint32_t r[32];
+              tc::tmem_ld32(t_o + c0, r);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * f);
+              tc::tmem_st32(t_o + c0, r);
+            }
+            tc::tmem_st_wait();
+          }
+        }
+        {
+          uint8_t* prow = sP + hl * 128;
+          const int c0 = 4 * w2 + 2 * part;   // 16-byte chunks of the row: 8 tokens each
+          *reinterpret_cast<uint4*>(prow + ((c0 ^ (hl & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+          *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (hl & 7)) << 4)) = make_uint4(p[4], p[5], p[6], p[7]);
+        }
+        // rows past the sequence end must not reach PV as NaN/Inf garbage
+        if (valid < kTile) {
+          uint8_t* stage = stages + (it % kPrStages) * kPrStageBytes;
+          const int nrow = kTile - valid;
+          for (int idx = threadIdx.x - 128; idx < nrow * 4 * 8; idx += 32 * kPrSoftmaxWarps) {
+            const int box = idx / (nrow * 8), rem = idx % (nrow * 8);
+            const int row = valid + rem / 8, ch = rem % 8;
+            *reinterpret_cast<uint4*>(stage + box * kPrBox + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(p_full);
+        ok = tc::named_sync_and(5, 32 * kPrSoftmaxWarps, good);
+      }
+      if (!ok) break;
+      // ---- segment epilogue: unnormalised O of this CTA's 64 heads, m and l
+      bool good = tc::mbar_wait(&S->o_done, (it - 1) & 1);
+      tc::tc_fence_after();
+      {
+        const int gh = 64 * static_cast<int>(rank) + o_head;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t r[32];
+          tc::tmem_ld32(t_o + c0, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(a.part_o + parto_index(slot, (o_lat0 + c0) / 4 + u, gh)) =
+                make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(o_free);
+      const float lw = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      S->red_l[w2][hl] = lw;
+      tc::named_sync(1 + q, 64);
+      if (w2 == 0 && part == 0) {
+        float2* ml = reinterpret_cast<float2*>(a.part_ml) + static_cast<int64_t>(slot) * kH +
+                     64 * static_cast<int>(rank) + hl;
+        *ml = make_float2(m_used, S->red_l[0][hl] + S->red_l[1][hl]);
+      }
+      ok = tc::named_sync_and(5, 32 * kPrSoftmaxWarps, good);
+    }
+    if (!ok) pr_set_abort(S);
+  }
+  // ---------------------------------------------------------------- teardown
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();   // no pair MMA, remote arrive or TMEM access of the other CTA is left
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc_pair<512>(tm);
+}
+
+}  // namespace tcd
+}  // namespace mla

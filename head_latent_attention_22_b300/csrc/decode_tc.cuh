@@ -103,10 +103,15 @@ __host__ __device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, in
 struct AbsorbArgs {
   const uint16_t* q_rope;     // [B, H, 64]
   const int32_t* seq_lens;    // [B]
-  uint16_t* q_lat;            // chunk-major, see qlat_index
+  uint16_t* q_lat;            // chunk-major (see qlat_index), or row-major [B, H, 576] when row_major
   Plan plan;
   int batch, nb, max_seq_len, ncl;
+  int row_major;
 };
+
+__host__ __device__ __forceinline__ int64_t qlat_row_index(int64_t b, int head, int k) {
+  return (b * kH + head) * kRow + k;
+}
 
 constexpr int kAbsorbThreads = 128;
 
@@ -218,7 +223,8 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
     for (int idx = threadIdx.x; idx < a.batch * 8; idx += kAbsorbThreads) {
       const int b = idx >> 3, c = idx & 7;
       const uint4 v = reinterpret_cast<const uint4*>(a.q_rope + (static_cast<int64_t>(b) * kH + i) * kDr)[c];
-      *reinterpret_cast<uint4*>(a.q_lat + qlat_index(b, kDc / 8 + c, i)) = v;
+      *reinterpret_cast<uint4*>(a.q_lat + (a.row_major ? qlat_row_index(b, i, kDc + 8 * c)
+                                                       : qlat_index(b, kDc / 8 + c, i))) = v;
     }
   }
   const uint32_t idesc = tc::idesc_bf16_f32(128, a.nb, 1, 0);
@@ -258,7 +264,8 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
           const int b = n0 + c0 + c;
           const int k = 256 * half + mt * 128 + 32 * warp + lane;   // latent element
           if (b < a.batch && ok)
-            a.q_lat[qlat_index(b, k >> 3, i) + (k & 7)] = f32_to_bf16_bits(__uint_as_float(r[c]));
+            a.q_lat[a.row_major ? qlat_row_index(b, i, k) : qlat_index(b, k >> 3, i) + (k & 7)] =
+                f32_to_bf16_bits(__uint_as_float(r[c]));
         }
       }
     }

@@ -8,6 +8,7 @@
 #include <string>
 
 #include "append.cuh"
+#include "attend_pair.cuh"
 #include "common.cuh"
 #include "decode_simt.cuh"
 #include "decode_tc.cuh"
@@ -267,27 +268,26 @@ constexpr size_t attend_smem() {
   return 1024 + tcd::AttendLayout<kF8>::kXbuf + 2 * tcd::kXbufBytes + sizeof(tcd::AttendSmem);
 }
 static_assert(attend_smem<false>() <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
+static_assert(tcd::kPrSmem <= 232448, "pair attend kernel shared memory exceeds the 227 KB a CTA may use");
 static_assert(attend_smem<true>() <= 232448, "attend kernel (FP8 cache) shared memory exceeds 227 KB");
 constexpr size_t kUvSmem = 1024 + tcd::kUvSmem;
 size_t absorb_smem(int nb) { return 1024 + 4 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
 
 struct TcDeviceState {
   bool ready = false;
-  int clusters[2] = {0, 0};   // bf16 cache, FP8 cache
+  int clusters[2] = {0, 0};   // bf16 cache (pair kernel), FP8 cache
 };
 std::mutex g_tc_mu;
 TcDeviceState g_tc_state[64];
 
-template <bool kF8>
-mla_status attend_setup(int* clusters) {
-  const void* fn = reinterpret_cast<const void*>(tcd::attend_tc_kernel<kF8>);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(attend_smem<kF8>()));
+// Number of two-CTA clusters of attend kernel `fn` (threads, shared memory) that fit on the GPU at once.
+mla_status cluster_count(const void* fn, int threads, size_t smem, int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return cuda_fail(e, "attend smem attribute");
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(2 * kMaxClusters);
-  lc.blockDim = dim3(tcd::kAttendThreads);
-  lc.dynamicSmemBytes = attend_smem<kF8>();
+  lc.blockDim = dim3(threads);
+  lc.dynamicSmemBytes = smem;
   int n = 0;
   if ((e = cudaOccupancyMaxActiveClusters(&n, fn, &lc)) != cudaSuccess || n < 1)
     return cuda_fail(e == cudaSuccess ? cudaErrorInvalidConfiguration : e, "attend cluster occupancy");
@@ -314,9 +314,12 @@ mla_status tc_device_setup(int* clusters) {
     if ((e = cudaFuncSetAttribute(tcd::uv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kUvSmem))) != cudaSuccess)
       return cuda_fail(e, "uv smem attribute");
-    mla_status s = attend_setup<false>(&st.clusters[0]);
+    mla_status s = cluster_count(reinterpret_cast<const void*>(tcd::attend_pair_kernel), tcd::kPrThreads,
+                                 tcd::kPrSmem, &st.clusters[0]);
     if (s != MLA_OK) return s;
-    if ((s = attend_setup<true>(&st.clusters[1])) != MLA_OK) return s;
+    if ((s = cluster_count(reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>), tcd::kAttendThreads,
+                           attend_smem<true>(), &st.clusters[1])) != MLA_OK)
+      return s;
     st.ready = true;
   }
   clusters[0] = st.clusters[0];
@@ -362,7 +365,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
-  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo;
+  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo, m_q;
   uint16_t* o_hi = reinterpret_cast<uint16_t*>(ws + p.off_hi);
   uint16_t* o_lo = reinterpret_cast<uint16_t*>(ws + p.off_lo);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -385,6 +388,9 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
     m_scale = m_lat;
     m_rope = m_lat;
     rope_x = tcd::kDc;
+    // the pair kernel reads Q_lat row-major [B * 128, 576] in boxes of 16 heads x 64 values
+    maps_ok = maps_ok && make_map_2d(&m_q, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH,
+                                     tcd::kRow * 2, 64, 16, SW);
   }
   if (!maps_ok ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
@@ -406,6 +412,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   aa.nb = p.nb;
   aa.max_seq_len = max_seq_len;
   aa.ncl = ncl;
+  aa.row_major = f8 ? 0 : 1;
 
   tcd::AttendArgs ta{};
   ta.q_lat = q_lat;
@@ -439,11 +446,15 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  absorb_smem(p.nb), st, absorb_args);
   if (s != MLA_OK) return s;
   stage_mark(1, st);
-  void* attend_args[] = {&m_lat, &m_scale, &m_rope, &ta};
-  s = launch_pdl(f8 ? reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>)
-                    : reinterpret_cast<const void*>(tcd::attend_tc_kernel<false>),
-                 dim3(2 * ncl), dim3(tcd::kAttendThreads), f8 ? attend_smem<true>() : attend_smem<false>(), st,
-                 attend_args);
+  if (f8) {
+    void* attend_args[] = {&m_lat, &m_scale, &m_rope, &ta};
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>), dim3(2 * ncl),
+                   dim3(tcd::kAttendThreads), attend_smem<true>(), st, attend_args);
+  } else {
+    void* attend_args[] = {&m_lat, &m_q, &ta};
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_pair_kernel), dim3(2 * ncl), dim3(tcd::kPrThreads),
+                   tcd::kPrSmem, st, attend_args);
+  }
   if (s != MLA_OK) return s;
   stage_mark(2, st);
   void* merge_args[] = {&ma};
