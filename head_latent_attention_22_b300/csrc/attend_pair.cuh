@@ -34,14 +34,15 @@
 namespace mla {
 namespace tcd {
 
-constexpr int kPrStages = 3;                        // cache tile ring depth
-constexpr int kPrBox = kTile * 128;                 // one TMA box: 64 rows x 64 bf16 = 8 KB
-constexpr int kPrStageBytes = 5 * kPrBox;           // 4 latent boxes + 1 rope box per CTA
+constexpr int kPrStages = 4;                        // cache tile ring depth
+constexpr int kPrBox = kTile * 128;                 // one latent TMA box: 64 rows x 64 bf16 = 8 KB (128-byte swizzle)
+constexpr int kPrRopeBox = kTile * 64;              // one rope box: 64 rows x 32 bf16 = 4 KB (64-byte swizzle)
+constexpr int kPrStageBytes = 4 * kPrBox + kPrRopeBox;   // this CTA's 256 latent and 32 rope columns of a tile
 constexpr int kPrQBox = 128 * 128;                  // 128 rows x 64 bf16 = 16 KB
-constexpr int kPrQBytes = 5 * kPrQBox;              // queries of 64 heads, both contraction halves
+constexpr int kPrQBytes = 4 * kPrQBox + 128 * 64;   // queries of 64 heads, both contraction halves (+ 32 rope each)
 constexpr int kPrPBytes = 64 * 128;                 // P: 64 heads x 64 tokens bf16
 constexpr int kPrSoftmaxWarps = 8;
-constexpr int kPrThreads = 32 * (4 + kPrSoftmaxWarps);   // TMA, MMA, forwarder, query loader, softmax
+constexpr int kPrThreads = 32 * (5 + kPrSoftmaxWarps);   // TMA, 2 MMA issuers, queries, forwarder, softmax
 constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
 constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
 constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
@@ -56,10 +57,12 @@ struct PairSmem {
   uint64_t p_full;             // even CTA: P written, O rescaled, tail rows cleared, in both CTAs
   uint64_t o_done;             // a PV completed (pair commit)
   uint64_t o_free;             // even CTA: both CTAs read O at a segment end
-  uint64_t drain;
-  float red_max[2][2][64];     // [tile parity][token half][head] row maxima of the two warps of a head
+  uint64_t drain[2];
+  union {
+    float red_max[2][2][64];   // [tile parity][token half][head] row maxima of the two warps of a head
+    float red_l[2][64];        // [token half][head] row sums at a segment end (after the last tile's maxima)
+  };
   float alpha[2][64];          // [tile parity][head] rescale factor of O (1 when unchanged)
-  float red_l[2][64];          // [token half][head] row sums at a segment end
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -74,15 +77,18 @@ __device__ __forceinline__ void pr_set_abort(PairSmem* s) {
   *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1;
 }
 
-// map_lat: the bf16 pool [rows, 576], boxes of 64 rows x 64 columns, 128-byte swizzle.
-// map_q:   Q_lat row-major [B * 128 heads, 576] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle.
+// map_lat:  the bf16 pool [rows, 576], boxes of 64 rows x 64 columns, 128-byte swizzle.
+// map_rope: the same pool, boxes of 64 rows x 32 columns, 64-byte swizzle.
+// map_q:    Q_lat row-major [B * 128 heads, 576] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle.
+// map_qr:   the same Q_lat, boxes of 16 rows x 32 columns, 64-byte swizzle.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
-    attend_pair_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_q,
+    attend_pair_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_rope,
+                       const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qr,
                        AttendArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = sm;                                   // 5 boxes [128 rows x 64]
-  uint8_t* stages = sm + kPrQBytes;                   // kPrStages x 5 boxes [64 tokens x 64]
+  uint8_t* sQ = sm;                                   // 4 boxes [128 rows x 64], 1 box [128 rows x 32]
+  uint8_t* stages = sm + kPrQBytes;                   // kPrStages x (4 boxes [64 tokens x 64], 1 [64 x 32])
   uint8_t* sP = stages + kPrStages * kPrStageBytes;   // [64 heads x 64 tokens]
   PairSmem* S = reinterpret_cast<PairSmem*>(sP + kPrPBytes);
 
@@ -106,11 +112,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     tc::mbar_init(&S->p_full, 2 * kPrSoftmaxWarps);
     tc::mbar_init(&S->o_done, 1);
     tc::mbar_init(&S->o_free, 2 * kPrSoftmaxWarps);
-    tc::mbar_init(&S->drain, 1);
+    tc::mbar_init(&S->drain[0], 1);
+    tc::mbar_init(&S->drain[1], 1);
     S->abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_map(&map_lat);
+    tc::tma_prefetch_map(&map_rope);
     tc::tma_prefetch_map(&map_q);
+    tc::tma_prefetch_map(&map_qr);
   }
   if (warp == 1) tc::tmem_alloc_pair<512>(&S->tmem_base);
   tc::tc_fence_before();
@@ -160,9 +169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
               for (int k = 0; k < 4; ++k)
                 tc::tma_load_2d_hint(dst + k * kPrBox, &map_lat, static_cast<int>(rank) * 256 + 64 * k, y,
                                      &S->full[st], policy);
-              // rope columns 32 rank .. 32 rank + 31 land in box columns 0..31 (the odd CTA's
-              // box reaches past the row end: those columns are filled with zeros)
-              tc::tma_load_2d_hint(dst + 4 * kPrBox, &map_lat, kDc + 32 * static_cast<int>(rank), y, &S->full[st],
+              tc::tma_load_2d_hint(dst + 4 * kPrBox, &map_rope, kDc + 32 * static_cast<int>(rank), y, &S->full[st],
                                    policy);
               ++it;
             }
@@ -179,76 +186,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
       for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kPrStages], (q / kPrStages) & 1);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- pair MMA issuer (even CTA)
+    // ---------------------------------------------------------------- score MMA issuer (even CTA)
+    // Scores and PVs go out from two threads, so the score MMAs of the next tile queue up
+    // while the PV of the current one waits for its probabilities.
     if (rank == 0 && lane == 0) {
       const uint32_t idesc_s = tc::idesc_bf16_f32(256, 128, 0, 0);
-      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);       // K-major Q, 128 rows
       const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), 16, 1024);   // K-major tile, 64 rows
+      const uint64_t qrdesc0 = tc::sdesc_sw64(tc::smem_u32(sQ + 4 * kPrQBox), 16, 512);        // rope part of Q
+      const uint64_t krdesc0 = tc::sdesc_sw64(tc::smem_u32(stages + 4 * kPrBox), 16, 512);     // rope box, stage 0
+      SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
+      int b, j0, j1;
+      uint32_t it = 0, seg = 0;
+      bool ok = true;
+      while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
+        ok = tc::mbar_wait(&S->qready, seg & 1);
+        for (int j = j0; j < j1 && ok; ++j, ++it) {
+          const uint32_t st = it % kPrStages;
+          ok = tc::mbar_wait(&S->ready[st], (it / kPrStages) & 1);
+          if (ok && it >= 2) ok = tc::mbar_wait(&S->s_free[it & 1], ((it - 2) >> 1) & 1);
+          if (!ok || pr_aborted(S)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t d = tm + kPrTmS + 128 * (it & 1);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int box = k >> 2, off = (k & 3) * 32;
+            const uint64_t ad = qdesc0 + static_cast<uint64_t>((box * kPrQBox + off) >> 4);
+            const uint64_t bd = kdesc0 + static_cast<uint64_t>((st * kPrStageBytes + box * kPrBox + off) >> 4);
+            tc::mma_ss_pair(d, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int k = 0; k < kPrKSteps - 16; ++k) {
+            const uint64_t ad = qrdesc0 + static_cast<uint64_t>((k * 32) >> 4);
+            const uint64_t bd = krdesc0 + static_cast<uint64_t>((st * kPrStageBytes + k * 32) >> 4);
+            tc::mma_ss_pair(d, ad, bd, idesc_s, 1u);
+          }
+          tc::mma_commit_pair(&S->s_full[it & 1]);
+          if (j == j1 - 1) tc::mma_commit_pair(&S->qfree);   // the queries may be replaced
+        }
+        ++seg;
+      }
+      if (!ok) pr_set_abort(S);
+      // every MMA issued so far must complete before TMEM is released
+      tc::mma_commit_pair(&S->drain[0]);
+      tc::mbar_wait(&S->drain[0], 0);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- PV MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), kPrBox, 1024);   // MN-major V
       const uint64_t pdesc0 = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);       // K-major P, 64 rows
       SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
       int b, j0, j1;
       uint32_t it = 0, seg = 0;
       bool ok = true;
-      // the PV of the previous tile goes out after the scores of the next one, so the
-      // softmax of a tile overlaps the score MMAs of the following tile
-      bool have_pv = false;
-      uint32_t pv_it = 0, pv_seg = 0;
-      bool pv_first = false;
-      auto issue_pv = [&]() -> bool {
-        if (!tc::mbar_wait_cl(&S->p_full, pv_it & 1)) return false;
-        if (pv_first && pv_seg > 0 && !tc::mbar_wait_cl(&S->o_free, (pv_seg - 1) & 1)) return false;
-        if (pr_aborted(S)) return false;
-        tc::tc_fence_after();
-        const uint32_t st = pv_it % kPrStages;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = pdesc0 + static_cast<uint64_t>((kk * 32) >> 4);
-            const uint64_t bd = vdesc0 + static_cast<uint64_t>((st * kPrStageBytes + 2 * h * kPrBox + kk * 2048) >> 4);
-            tc::mma_ss_pair(tm + kPrTmO + 128 * h, ad, bd, idesc_o, (pv_first && kk == 0) ? 0u : 1u);
-          }
-        }
-        tc::mma_commit_pair(&S->o_done);
-        tc::mma_commit_pair(&S->empty[st]);
-        return true;
-      };
       while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
-        ok = tc::mbar_wait_cl(&S->qready, seg & 1);
         for (int j = j0; j < j1 && ok; ++j, ++it) {
-          const uint32_t st = it % kPrStages;
-          ok = tc::mbar_wait_cl(&S->ready[st], (it / kPrStages) & 1);
-          if (ok && it >= 2) ok = tc::mbar_wait_cl(&S->s_free[it & 1], ((it - 2) >> 1) & 1);
+          ok = tc::mbar_wait(&S->p_full, it & 1);
+          if (ok && j == j0 && seg > 0) ok = tc::mbar_wait(&S->o_free, (seg - 1) & 1);
           if (!ok || pr_aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
-          const uint32_t d = tm + kPrTmS + 128 * (it & 1);
+          const uint32_t st = it % kPrStages;
 #pragma unroll
-          for (int k = 0; k < kPrKSteps; ++k) {
-            const int box = k < 16 ? (k >> 2) : 4;
-            const int off = (k < 16 ? (k & 3) : (k - 16)) * 32;
-            const uint64_t ad = qdesc0 + static_cast<uint64_t>((box * kPrQBox + off) >> 4);
-            const uint64_t bd = kdesc0 + static_cast<uint64_t>((st * kPrStageBytes + box * kPrBox + off) >> 4);
-            tc::mma_ss_pair(d, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = pdesc0 + static_cast<uint64_t>((kk * 32) >> 4);
+              const uint64_t bd =
+                  vdesc0 + static_cast<uint64_t>((st * kPrStageBytes + 2 * h * kPrBox + kk * 2048) >> 4);
+              tc::mma_ss_pair(tm + kPrTmO + 128 * h, ad, bd, idesc_o, (j == j0 && kk == 0) ? 0u : 1u);
+            }
           }
-          tc::mma_commit_pair(&S->s_full[it & 1]);
-          if (j == j1 - 1) tc::mma_commit_pair(&S->qfree);   // the queries may be replaced
-          if (have_pv && !issue_pv()) { ok = false; break; }
-          have_pv = true;
-          pv_it = it;
-          pv_seg = seg;
-          pv_first = j == j0;
+          tc::mma_commit_pair(&S->o_done);
+          tc::mma_commit_pair(&S->empty[st]);
         }
         ++seg;
       }
-      if (ok && have_pv) ok = issue_pv();
       if (!ok) pr_set_abort(S);
-      // every MMA issued so far must complete before TMEM is released
-      tc::mma_commit_pair(&S->drain);
-      tc::mbar_wait(&S->drain, 0);
+      tc::mma_commit_pair(&S->drain[1]);
+      tc::mbar_wait(&S->drain[1], 0);
     }
-  } else if (warp == 2) {
+  } else if (warp == 4) {
     // ---------------------------------------------------------------- tile forwarder (both CTAs)
     // tells the even CTA's MMA issuer that this CTA's half of a tile has landed
     if (lane == 0) {
@@ -278,10 +297,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         tc::mbar_arrive_expect_tx(&S->qfull, kPrQBytes);
         const int row0 = b * kH + 64 * static_cast<int>(rank);
         for (int q = 0; q < 4; ++q)
-          for (int half = 0; half < 2; ++half)
-            for (int k = 0; k < 5; ++k)
-              tc::tma_load_2d(sQ + k * kPrQBox + (32 * q + 16 * half) * 128, &map_q,
-                              k < 4 ? 256 * half + 64 * k : kDc + 32 * half, row0 + 16 * q, &S->qfull);
+          for (int half = 0; half < 2; ++half) {
+            const int r = 32 * q + 16 * half;   // first of the 16 rows of (quarter q, contraction half)
+            for (int k = 0; k < 4; ++k)
+              tc::tma_load_2d(sQ + k * kPrQBox + r * 128, &map_q, 256 * half + 64 * k, row0 + 16 * q, &S->qfull);
+            tc::tma_load_2d(sQ + 4 * kPrQBox + r * 64, &map_qr, kDc + 32 * half, row0 + 16 * q, &S->qfull);
+          }
         ok = tc::mbar_wait(&S->qfull, seg & 1);
         if (!ok) break;
         tc::mbar_arrive_cluster(qready);
@@ -291,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax + segment epilogue
-    const int q = warp & 3, w2 = (warp - 4) >> 2;     // lane quarter; token half (32 w2 .. 32 w2 + 31)
+    const int q = warp & 3, w2 = (warp - 5) >> 2;     // lane quarter; token half (32 w2 .. 32 w2 + 31)
     const int hl = 16 * q + (lane & 15);              // this CTA's head whose scores this thread finishes
     const int part = lane >> 4;                       // which 16 of the warp's 32 tokens it finishes
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -328,7 +349,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
           tc::tmem_ld_wait();
           tc::tc_fence_before();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive_cluster(s_free0 + 8u * (it & 1));
+          if (lane == 0) tc::mbar_arrive_cluster_relaxed(s_free0 + 8u * (it & 1));
           // the two halves of a head sit in lanes i and i + 16 of the warp: swap the 16 tokens
           // each of them finishes
 #pragma unroll
@@ -406,7 +427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         if (valid < kTile) {
           uint8_t* stage = stages + (it % kPrStages) * kPrStageBytes;
           const int nrow = kTile - valid;
-          for (int idx = threadIdx.x - 128; idx < nrow * 4 * 8; idx += 32 * kPrSoftmaxWarps) {
+          for (int idx = threadIdx.x - 160; idx < nrow * 4 * 8; idx += 32 * kPrSoftmaxWarps) {
             const int box = idx / (nrow * 8), rem = idx % (nrow * 8);
             const int row = valid + rem / 8, ch = rem % 8;
             *reinterpret_cast<uint4*>(stage + box * kPrBox + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);

@@ -365,7 +365,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
-  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo, m_q;
+  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo, m_q, m_qr, m_rope32;
   uint16_t* o_hi = reinterpret_cast<uint16_t*>(ws + p.off_hi);
   uint16_t* o_lo = reinterpret_cast<uint16_t*>(ws + p.off_lo);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -388,9 +388,16 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
     m_scale = m_lat;
     m_rope = m_lat;
     rope_x = tcd::kDc;
-    // the pair kernel reads Q_lat row-major [B * 128, 576] in boxes of 16 heads x 64 values
-    maps_ok = maps_ok && make_map_2d(&m_q, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH,
-                                     tcd::kRow * 2, 64, 16, SW);
+    // the pair kernel reads Q_lat row-major [B * 128, 576] in boxes of 16 heads x 64 values (latent) and
+    // 16 heads x 32 values (rope), and the pool's rope columns in boxes of 64 rows x 32 values
+    const CUtensorMapSwizzle SW64 = CU_TENSOR_MAP_SWIZZLE_64B;
+    maps_ok = maps_ok &&
+              make_map_2d(&m_q, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 64, 16,
+                          SW) &&
+              make_map_2d(&m_qr, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 32, 16,
+                          SW64) &&
+              make_map_2d(&m_rope32, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 32,
+                          tcd::kTile, SW64);
   }
   if (!maps_ok ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
@@ -451,7 +458,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
     s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>), dim3(2 * ncl),
                    dim3(tcd::kAttendThreads), attend_smem<true>(), st, attend_args);
   } else {
-    void* attend_args[] = {&m_lat, &m_q, &ta};
+    void* attend_args[] = {&m_lat, &m_rope32, &m_q, &m_qr, &ta};
     s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_pair_kernel), dim3(2 * ncl), dim3(tcd::kPrThreads),
                    tcd::kPrSmem, st, attend_args);
   }
