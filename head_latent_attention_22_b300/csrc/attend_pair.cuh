@@ -40,7 +40,10 @@ constexpr int kPrRopeBox = kTile * 64;              // one rope box: 64 rows x 3
 constexpr int kPrStageBytes = 4 * kPrBox + kPrRopeBox;   // this CTA's 256 latent and 32 rope columns of a tile
 constexpr int kPrQBox = 128 * 128;                  // 128 rows x 64 bf16 = 16 KB
 constexpr int kPrQBytes = 4 * kPrQBox + 128 * 64;   // queries of 64 heads, both contraction halves (+ 32 rope each)
-constexpr int kPrPBytes = 64 * 128;                 // P: 64 heads x 64 tokens bf16
+constexpr int kPrPHalf = 64 * 64;                   // P of 32 tokens: 64 heads x 32 bf16 (64-byte swizzle)
+// P of a tile: tokens 0..31 go into the tile's rope box (dead once its score MMAs completed),
+// tokens 32..63 into one of two 4 KB buffers (by tile parity)
+constexpr int kPrPBytes = 2 * kPrPHalf;
 constexpr int kPrSoftmaxWarps = 8;
 constexpr int kPrThreads = 32 * (5 + kPrSoftmaxWarps);   // TMA, 2 MMA issuers, queries, forwarder, softmax
 constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
@@ -54,8 +57,8 @@ struct PairSmem {
   uint64_t qfull, qfree, qready;
   uint64_t s_full[2];          // scores of a tile are in TMEM (pair commit)
   uint64_t s_free[2];          // even CTA: all softmax warps of both CTAs read them
-  uint64_t p_full;             // even CTA: P written, O rescaled, tail rows cleared, in both CTAs
-  uint64_t o_done;             // a PV completed (pair commit)
+  uint64_t p_full[2];          // even CTA, by tile parity: P written, O rescaled, tail rows cleared, in both CTAs
+  uint64_t o_done[2];          // the PV of a tile of this parity completed (pair commit)
   uint64_t o_free;             // even CTA: both CTAs read O at a segment end
   uint64_t drain[2];
   union {
@@ -89,7 +92,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = sm;                                   // 4 boxes [128 rows x 64], 1 box [128 rows x 32]
   uint8_t* stages = sm + kPrQBytes;                   // kPrStages x (4 boxes [64 tokens x 64], 1 [64 x 32])
-  uint8_t* sP = stages + kPrStages * kPrStageBytes;   // [64 heads x 64 tokens]
+  uint8_t* sP = stages + kPrStages * kPrStageBytes;   // 2 x [64 heads x 32 tokens] (P tokens 32..63)
   PairSmem* S = reinterpret_cast<PairSmem*>(sP + kPrPBytes);
 
   const uint32_t rank = tc::cluster_ctarank();
@@ -109,8 +112,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
       tc::mbar_init(&S->s_full[b], 1);
       tc::mbar_init(&S->s_free[b], 2 * kPrSoftmaxWarps);
     }
-    tc::mbar_init(&S->p_full, 2 * kPrSoftmaxWarps);
-    tc::mbar_init(&S->o_done, 1);
+    tc::mbar_init(&S->p_full[0], 2 * kPrSoftmaxWarps);
+    tc::mbar_init(&S->p_full[1], 2 * kPrSoftmaxWarps);
+    tc::mbar_init(&S->o_done[0], 1);
+    tc::mbar_init(&S->o_done[1], 1);
     tc::mbar_init(&S->o_free, 2 * kPrSoftmaxWarps);
     tc::mbar_init(&S->drain[0], 1);
     tc::mbar_init(&S->drain[1], 1);
@@ -236,14 +241,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     if (rank == 0 && lane == 0) {
       const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), kPrBox, 1024);   // MN-major V
-      const uint64_t pdesc0 = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);       // K-major P, 64 rows
+      const uint64_t plo0 = tc::sdesc_sw64(tc::smem_u32(stages + 4 * kPrBox), 16, 512);   // P tokens 0..31, stage 0
+      const uint64_t phi0 = tc::sdesc_sw64(tc::smem_u32(sP), 16, 512);                    // P tokens 32..63, buffer 0
       SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
       int b, j0, j1;
       uint32_t it = 0, seg = 0;
       bool ok = true;
       while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
         for (int j = j0; j < j1 && ok; ++j, ++it) {
-          ok = tc::mbar_wait(&S->p_full, it & 1);
+          // one barrier per tile parity: the softmax may finish tile it + 1 before this thread
+          // has seen tile it complete, but not tile it + 2 (its P buffer is read by PV(it))
+          ok = tc::mbar_wait(&S->p_full[it & 1], (it >> 1) & 1);
           if (ok && j == j0 && seg > 0) ok = tc::mbar_wait(&S->o_free, (seg - 1) & 1);
           if (!ok || pr_aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
@@ -252,13 +260,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
           for (int h = 0; h < 2; ++h) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = pdesc0 + static_cast<uint64_t>((kk * 32) >> 4);
+              const uint64_t ad = kk < 2 ? plo0 + static_cast<uint64_t>((st * kPrStageBytes + kk * 32) >> 4)
+                                         : phi0 + static_cast<uint64_t>(((it & 1) * kPrPHalf + (kk - 2) * 32) >> 4);
               const uint64_t bd =
                   vdesc0 + static_cast<uint64_t>((st * kPrStageBytes + 2 * h * kPrBox + kk * 2048) >> 4);
               tc::mma_ss_pair(tm + kPrTmO + 128 * h, ad, bd, idesc_o, (j == j0 && kk == 0) ? 0u : 1u);
             }
           }
-          tc::mma_commit_pair(&S->o_done);
+          tc::mma_commit_pair(&S->o_done[it & 1]);
           tc::mma_commit_pair(&S->empty[st]);
         }
         ++seg;
@@ -317,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     const int part = lane >> 4;                       // which 16 of the warp's 32 tokens it finishes
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t s_free0 = tc::map_peer(&S->s_free[0], 0);
-    const uint32_t p_full = tc::map_peer(&S->p_full, 0);
+    const uint32_t p_full0 = tc::map_peer(&S->p_full[0], 0);
     const uint32_t o_free = tc::map_peer(&S->o_free, 0);
     const float sl = a.scale_log2;
     // O lanes this thread reads or rescales: lane 32 q + lane holds head (32 q + lane) mod 64 of this
@@ -398,10 +407,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         }
         l += ps[0] + ps[1];
         if (lane < 16) S->alpha[it & 1][hl] = alpha;
-        // the PV of the previous tile must be done: P and O are ours
-        if (it > 0) good = tc::mbar_wait(&S->o_done, (it - 1) & 1) && good;
+        // the second half of P goes into the buffer the PV two tiles back read
+        if (it > 1) good = tc::mbar_wait(&S->o_done[it & 1], ((it - 2) >> 1) & 1) && good;
         tc::tc_fence_after();
         if (tc::named_sync_or(5, 32 * kPrSoftmaxWarps, resc)) {
+          // O must not be in use: the PV of the previous tile completes first
+          if (it > 0) good = tc::mbar_wait(&S->o_done[(it - 1) & 1], ((it - 1) >> 1) & 1) && good;
+          tc::tc_fence_after();
           // a head's O rows are lanes h and h + 64: the threads on those lanes rescale them
           const float f = S->alpha[it & 1][o_head];
           if (__any_sync(0xffffffffu, f != 1.f)) {
@@ -418,10 +430,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
           }
         }
         {
-          uint8_t* prow = sP + hl * 128;
-          const int c0 = 4 * w2 + 2 * part;   // 16-byte chunks of the row: 8 tokens each
-          *reinterpret_cast<uint4*>(prow + ((c0 ^ (hl & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
-          *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ (hl & 7)) << 4)) = make_uint4(p[4], p[5], p[6], p[7]);
+          // 64-byte rows, 64-byte swizzle: chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
+          uint8_t* prow = (w2 == 0 ? stages + (it % kPrStages) * kPrStageBytes + 4 * kPrBox
+                                   : sP + (it & 1) * kPrPHalf) + hl * 64;
+          const int c0 = 2 * part, x = (hl >> 1) & 3;   // 16-byte chunks of the row: 8 tokens each
+          *reinterpret_cast<uint4*>(prow + ((c0 ^ x) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+          *reinterpret_cast<uint4*>(prow + (((c0 + 1) ^ x) << 4)) = make_uint4(p[4], p[5], p[6], p[7]);
         }
         // rows past the sequence end must not reach PV as NaN/Inf garbage
         if (valid < kTile) {
@@ -436,12 +450,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive_cluster(p_full);
+        if (lane == 0) tc::mbar_arrive_cluster(p_full0 + 8u * (it & 1));
         ok = tc::named_sync_and(5, 32 * kPrSoftmaxWarps, good);
       }
       if (!ok) break;
       // ---- segment epilogue: unnormalised O of this CTA's 64 heads, m and l
-      bool good = tc::mbar_wait(&S->o_done, (it - 1) & 1);
+      bool good = tc::mbar_wait(&S->o_done[(it - 1) & 1], ((it - 1) >> 1) & 1);
       tc::tc_fence_after();
       {
         const int gh = 64 * static_cast<int>(rank) + o_head;
