@@ -45,7 +45,7 @@ constexpr int kPrPHalf = 64 * 64;                   // P of 32 tokens: 64 heads 
 // tokens 32..63 into one of two 4 KB buffers (by tile parity)
 constexpr int kPrPBytes = 2 * kPrPHalf;
 constexpr int kPrSoftmaxWarps = 8;
-constexpr int kPrThreads = 32 * (5 + kPrSoftmaxWarps);   // TMA, 2 MMA issuers, queries, forwarder, softmax
+constexpr int kPrThreads = 32 * (6 + kPrSoftmaxWarps);   // TMA, 3 MMA issuers, queries, forwarder, softmax
 constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
 constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
 constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
@@ -60,7 +60,7 @@ struct PairSmem {
   uint64_t p_full[2];          // even CTA, by tile parity: P written, O rescaled, tail rows cleared, in both CTAs
   uint64_t o_done[2];          // the PV of a tile of this parity completed (pair commit)
   uint64_t o_free;             // even CTA: both CTAs read O at a segment end
-  uint64_t drain[2];
+  uint64_t drain[3];
   union {
     float red_max[2][2][64];   // [tile parity][token half][head] row maxima of the two warps of a head
     float red_l[2][64];        // [token half][head] row sums at a segment end (after the last tile's maxima)
@@ -106,7 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
       tc::mbar_init(&S->ready[s], 2);
     }
     tc::mbar_init(&S->qfull, 1);
-    tc::mbar_init(&S->qfree, 1);
+    tc::mbar_init(&S->qfree, 2);   // one commit from each score issuer
     tc::mbar_init(&S->qready, 2);
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&S->s_full[b], 1);
@@ -117,8 +117,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     tc::mbar_init(&S->o_done[0], 1);
     tc::mbar_init(&S->o_done[1], 1);
     tc::mbar_init(&S->o_free, 2 * kPrSoftmaxWarps);
-    tc::mbar_init(&S->drain[0], 1);
-    tc::mbar_init(&S->drain[1], 1);
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&S->drain[i], 1);
     S->abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_map(&map_lat);
@@ -190,11 +189,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
       const uint32_t first = it > kPrStages ? it - kPrStages : 0;
       for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kPrStages], (q / kPrStages) & 1);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- score MMA issuer (even CTA)
-    // Scores and PVs go out from two threads, so the score MMAs of the next tile queue up
-    // while the PV of the current one waits for its probabilities.
+  } else if (warp == 1 || warp == 5) {
+    // ---------------------------------------------------------------- score MMA issuers (even CTA)
+    // Scores go out from two threads, warp 1 for even tiles and warp 5 for odd ones, and PVs
+    // from a third: the tensor pipe stays fed while one thread waits or loops.
     if (rank == 0 && lane == 0) {
+      const uint32_t mine = warp == 1 ? 0u : 1u;   // tile parity this thread issues
       const uint32_t idesc_s = tc::idesc_bf16_f32(256, 128, 0, 0);
       const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);       // K-major Q, 128 rows
       const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), 16, 1024);   // K-major tile, 64 rows
@@ -207,6 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
       while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
         ok = tc::mbar_wait(&S->qready, seg & 1);
         for (int j = j0; j < j1 && ok; ++j, ++it) {
+          if ((it & 1u) != mine) continue;
           const uint32_t st = it % kPrStages;
           ok = tc::mbar_wait(&S->ready[st], (it / kPrStages) & 1);
           if (ok && it >= 2) ok = tc::mbar_wait(&S->s_free[it & 1], ((it - 2) >> 1) & 1);
@@ -227,14 +228,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
             tc::mma_ss_pair(d, ad, bd, idesc_s, 1u);
           }
           tc::mma_commit_pair(&S->s_full[it & 1]);
-          if (j == j1 - 1) tc::mma_commit_pair(&S->qfree);   // the queries may be replaced
         }
+        // the queries may be replaced once both threads' score MMAs of the segment completed
+        if (ok) tc::mma_commit_pair(&S->qfree);
         ++seg;
       }
       if (!ok) pr_set_abort(S);
       // every MMA issued so far must complete before TMEM is released
-      tc::mma_commit_pair(&S->drain[0]);
-      tc::mbar_wait(&S->drain[0], 0);
+      tc::mma_commit_pair(&S->drain[mine]);
+      tc::mbar_wait(&S->drain[mine], 0);
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------------- PV MMA issuer (even CTA)
@@ -273,8 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         ++seg;
       }
       if (!ok) pr_set_abort(S);
-      tc::mma_commit_pair(&S->drain[1]);
-      tc::mbar_wait(&S->drain[1], 0);
+      tc::mma_commit_pair(&S->drain[2]);
+      tc::mbar_wait(&S->drain[2], 0);
     }
   } else if (warp == 4) {
     // ---------------------------------------------------------------- tile forwarder (both CTAs)
@@ -321,7 +323,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax + segment epilogue
-    const int q = warp & 3, w2 = (warp - 5) >> 2;     // lane quarter; token half (32 w2 .. 32 w2 + 31)
+    const int q = warp & 3, w2 = (warp - 6) >> 2;     // lane quarter; token half (32 w2 .. 32 w2 + 31)
     const int hl = 16 * q + (lane & 15);              // this CTA's head whose scores this thread finishes
     const int part = lane >> 4;                       // which 16 of the warp's 32 tokens it finishes
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -441,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         if (valid < kTile) {
           uint8_t* stage = stages + (it % kPrStages) * kPrStageBytes;
           const int nrow = kTile - valid;
-          for (int idx = threadIdx.x - 160; idx < nrow * 4 * 8; idx += 32 * kPrSoftmaxWarps) {
+          for (int idx = threadIdx.x - 192; idx < nrow * 4 * 8; idx += 32 * kPrSoftmaxWarps) {
             const int box = idx / (nrow * 8), rem = idx % (nrow * 8);
             const int row = valid + rem / 8, ch = rem % 8;
             *reinterpret_cast<uint4*>(stage + box * kPrBox + row * 128 + ch * 16) = make_uint4(0, 0, 0, 0);

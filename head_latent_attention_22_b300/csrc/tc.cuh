@@ -77,14 +77,29 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, letting the hardware suspend the thread for up to `hint_ns` while the
+// phase is incomplete (it resumes when the phase completes), so waiting warps
+// leave their issue slots to the warps that share the scheduler.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with parity `parity` of `bar` has completed. Returns
 // false (and sets the timeout bit) if that takes longer than kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test(bar, parity)) return true;
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test_sleep(bar, parity, 20000u)) return true;
     if (global_ns() - t0 > kWaitLimitNs) {
       flag_error(ERR_BIT_TIMEOUT);
       return false;
