@@ -34,7 +34,7 @@
 namespace mla {
 namespace tcd {
 
-constexpr int kPrStages = 4;                        // cache tile ring depth
+constexpr int kPrMaxStages = 4;                     // cache tile ring depth (bf16 cache; 3 with FP8)
 constexpr int kPrBox = kTile * 128;                 // one latent TMA box: 64 rows x 64 bf16 = 8 KB (128-byte swizzle)
 constexpr int kPrRopeBox = kTile * 64;              // one rope box: 64 rows x 32 bf16 = 4 KB (64-byte swizzle)
 constexpr int kPrStageBytes = 4 * kPrBox + kPrRopeBox;   // this CTA's 256 latent and 32 rope columns of a tile
@@ -45,15 +45,16 @@ constexpr int kPrPHalf = 64 * 64;                   // P of 32 tokens: 64 heads 
 // tokens 32..63 into one of two 4 KB buffers (by tile parity)
 constexpr int kPrPBytes = 2 * kPrPHalf;
 constexpr int kPrSoftmaxWarps = 8;
-constexpr int kPrThreads = 32 * (6 + kPrSoftmaxWarps);   // TMA, 3 MMA issuers, queries, forwarder, softmax
 constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
 constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
 constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
 
 struct PairSmem {
-  uint64_t full[kPrStages];    // this CTA's half of a tile landed (TMA)
-  uint64_t empty[kPrStages];   // the PV of the tile in the slot completed (pair commit)
-  uint64_t ready[kPrStages];   // even CTA: both halves of a tile landed (one arrival per CTA)
+  uint64_t full[kPrMaxStages];    // this CTA's half of a tile landed (TMA; bf16 cache)
+  uint64_t empty[kPrMaxStages];   // the PV of the tile in the slot completed (pair commit)
+  uint64_t ready[kPrMaxStages];   // even CTA: both halves of a tile are in their bf16 stages
+  uint64_t raw_full[2];           // FP8 cache: codes, scales and rope values of a tile landed
+  uint64_t raw_empty[2];          // FP8 cache: the dequantising warps are done with a raw slot
   uint64_t qfull, qfree, qready;
   uint64_t s_full[2];          // scores of a tile are in TMEM (pair commit)
   uint64_t s_free[2];          // even CTA: all softmax warps of both CTAs read them
@@ -70,8 +71,20 @@ struct PairSmem {
   int32_t abort_flag;
 };
 
-constexpr size_t kPrSmem = 1024 + kPrQBytes + static_cast<size_t>(kPrStages) * kPrStageBytes + kPrPBytes +
-                           sizeof(PairSmem);
+// Per cache format: ring depths, thread count and shared-memory carve-up
+// (Q | bf16 stages | FP8 raw ring | P tokens 32..63 | barriers).
+template <bool kF8>
+struct PairCfg {
+  static constexpr int kSt = kF8 ? 3 : kPrMaxStages;
+  static constexpr int kRaw = kF8 ? 2 : 0;
+  static constexpr int kRawCodes = kTile * 256;                 // this CTA's 256 E4M3 codes of 64 rows
+  static constexpr int kRawBytes = kRawCodes + kTile * 16;      // + the 4 fp32 block scales of each row
+  static constexpr int kDequantWarps = kF8 ? 4 : 0;
+  static constexpr int kThreads = 32 * (6 + kPrSoftmaxWarps + kDequantWarps);
+  static constexpr size_t kRawOff = kPrQBytes + static_cast<size_t>(kSt) * kPrStageBytes;
+  static constexpr size_t kPOff = kRawOff + static_cast<size_t>(kRaw) * kRawBytes;
+  static constexpr size_t kSmem = 1024 + kPOff + kPrPBytes + sizeof(PairSmem);
+};
 
 __device__ __forceinline__ bool pr_aborted(const PairSmem* s) {
   return *reinterpret_cast<const volatile int32_t*>(&s->abort_flag) != 0;
@@ -80,19 +93,30 @@ __device__ __forceinline__ void pr_set_abort(PairSmem* s) {
   *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1;
 }
 
-// map_lat:  the bf16 pool [rows, 576], boxes of 64 rows x 64 columns, 128-byte swizzle.
-// map_rope: the same pool, boxes of 64 rows x 32 columns, 64-byte swizzle.
-// map_q:    Q_lat row-major [B * 128 heads, 576] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle.
-// map_qr:   the same Q_lat, boxes of 16 rows x 32 columns, 64-byte swizzle.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
+// bf16 cache (kF8 = false):
+//   map_lat:   the pool [rows, 576], boxes of 64 rows x 64 columns, 128-byte swizzle.
+//   map_rope:  the same pool, boxes of 64 rows x 32 columns, 64-byte swizzle.
+// FP8 cache (kF8 = true; rows of 512 E4M3 codes, 4 fp32 scales, 64 bf16 rope values):
+//   map_lat:   byte view of the pool [rows, 656], unswizzled boxes of 64 rows x 256 codes.
+//   map_scale: the same, boxes of 64 rows x 16 bytes (the 4 block scales).
+//   map_rope:  the rope values as bf16 [rows, 64] (row stride 656 bytes), boxes of 64 x 32, 64-byte swizzle.
+// map_q:  Q_lat row-major [B * 128 heads, 576] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle.
+// map_qr: the same Q_lat, boxes of 16 rows x 32 columns, 64-byte swizzle.
+// The FP8 codes are dequantised (code x block scale, rounded to bf16) by four extra warps into the
+// same bf16 tile layout a bf16 pool gives, so the MMAs and the softmax do not depend on the format.
+template <bool kF8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThreads, 1)
     attend_pair_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_rope,
                        const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_qr,
-                       AttendArgs a) {
+                       const __grid_constant__ CUtensorMap map_scale, AttendArgs a) {
+  using CF = PairCfg<kF8>;
+  constexpr int kPrStages = CF::kSt;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = sm;                                   // 4 boxes [128 rows x 64], 1 box [128 rows x 32]
   uint8_t* stages = sm + kPrQBytes;                   // kPrStages x (4 boxes [64 tokens x 64], 1 [64 x 32])
-  uint8_t* sP = stages + kPrStages * kPrStageBytes;   // 2 x [64 heads x 32 tokens] (P tokens 32..63)
+  uint8_t* rawb = sm + CF::kRawOff;                   // FP8: 2 x (codes [64 x 256], scales [64 x 16])
+  uint8_t* sP = sm + CF::kPOff;                       // 2 x [64 heads x 32 tokens] (P tokens 32..63)
   PairSmem* S = reinterpret_cast<PairSmem*>(sP + kPrPBytes);
 
   const uint32_t rank = tc::cluster_ctarank();
@@ -103,7 +127,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     for (int s = 0; s < kPrStages; ++s) {
       tc::mbar_init(&S->full[s], 1);
       tc::mbar_init(&S->empty[s], 1);
-      tc::mbar_init(&S->ready[s], 2);
+      tc::mbar_init(&S->ready[s], kF8 ? 2 * CF::kDequantWarps : 2);
+    }
+    for (int s = 0; s < CF::kRaw; ++s) {
+      tc::mbar_init(&S->raw_full[s], 1);
+      tc::mbar_init(&S->raw_empty[s], CF::kDequantWarps);
     }
     tc::mbar_init(&S->qfull, 1);
     tc::mbar_init(&S->qfree, 2);   // one commit from each score issuer
@@ -124,6 +152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     tc::tma_prefetch_map(&map_rope);
     tc::tma_prefetch_map(&map_q);
     tc::tma_prefetch_map(&map_qr);
+    if (kF8) tc::tma_prefetch_map(&map_scale);
   }
   if (warp == 1) tc::tmem_alloc_pair<512>(&S->tmem_base);
   tc::tc_fence_before();
@@ -166,8 +195,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
           if (lane == 0 && ok) {
             const int st = it % kPrStages;
             if (it >= kPrStages) ok = tc::mbar_wait(&S->empty[st], ((it / kPrStages) - 1) & 1);
+            if (kF8 && ok && it >= 2) ok = tc::mbar_wait(&S->raw_empty[it & 1], ((it / 2) - 1) & 1);
             if (ok && pr_aborted(S)) ok = false;
-            if (ok) {
+            if (ok && kF8) {
+              // codes and scales into the raw ring, the bf16 rope values straight into the stage
+              uint8_t* raw = rawb + (it & 1) * CF::kRawBytes;
+              uint64_t* bar = &S->raw_full[it & 1];
+              tc::mbar_arrive_expect_tx(bar, CF::kRawBytes + kPrRopeBox);
+              tc::tma_load_2d_hint(raw, &map_lat, static_cast<int>(rank) * 256, y, bar, policy);
+              tc::tma_load_2d_hint(raw + CF::kRawCodes, &map_scale, kDc, y, bar, policy);
+              tc::tma_load_2d_hint(stages + st * kPrStageBytes + 4 * kPrBox, &map_rope, 32 * static_cast<int>(rank), y,
+                                   bar, policy);
+            } else if (ok) {
               uint8_t* dst = stages + st * kPrStageBytes;
               tc::mbar_arrive_expect_tx(&S->full[st], kPrStageBytes);
               for (int k = 0; k < 4; ++k)
@@ -175,8 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
                                      &S->full[st], policy);
               tc::tma_load_2d_hint(dst + 4 * kPrBox, &map_rope, kDc + 32 * static_cast<int>(rank), y, &S->full[st],
                                    policy);
-              ++it;
             }
+            if (ok) ++it;
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
@@ -186,8 +225,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
     it = __shfl_sync(0xffffffffu, it, 0);
     if (lane == 0) {
       if (!ok) pr_set_abort(S);
-      const uint32_t first = it > kPrStages ? it - kPrStages : 0;
-      for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kPrStages], (q / kPrStages) & 1);
+      // copies still in flight must land before the CTA exits
+      if (kF8) {
+        const uint32_t first = it > 2 ? it - 2 : 0;
+        for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->raw_full[q & 1], (q / 2) & 1);
+      } else {
+        const uint32_t first = it > kPrStages ? it - kPrStages : 0;
+        for (uint32_t q = first; q < it; ++q) tc::mbar_wait(&S->full[q % kPrStages], (q / kPrStages) & 1);
+      }
     }
   } else if (warp == 1 || warp == 5) {
     // ---------------------------------------------------------------- score MMA issuers (even CTA)
@@ -279,9 +324,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
       tc::mbar_wait(&S->drain[2], 0);
     }
   } else if (warp == 4) {
-    // ---------------------------------------------------------------- tile forwarder (both CTAs)
+    // ---------------------------------------------------------------- tile forwarder (both CTAs, bf16)
     // tells the even CTA's MMA issuer that this CTA's half of a tile has landed
-    if (lane == 0) {
+    if (!kF8 && lane == 0) {
       const uint32_t ready0 = tc::map_peer(&S->ready[0], 0);
       for (uint32_t it = 0; it < n_share; ++it) {
         const uint32_t st = it % kPrStages;
@@ -320,6 +365,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPrThreads, 1)
         ++seg;
       }
       if (!ok) pr_set_abort(S);
+    }
+  } else if (kF8 && warp >= 6 + kPrSoftmaxWarps) {
+    // ---------------------------------------------------------------- FP8: dequantise (both CTAs)
+    // tile it's raw rows -> its bf16 stage: value = E4M3 code x block scale, rounded to bf16,
+    // written in the 128-byte swizzled layout of a bf16 tile; 2,048 chunks of 8 values per tile
+    const int dt = static_cast<int>(threadIdx.x) - 32 * (6 + kPrSoftmaxWarps);   // 0 .. 127
+    const uint32_t ready0 = tc::map_peer(&S->ready[0], 0);
+    for (uint32_t it = 0; it < n_share; ++it) {
+      const uint32_t st = it % kPrStages;
+      if (!tc::mbar_wait(&S->raw_full[it & 1], (it / 2) & 1) || pr_aborted(S)) {
+        pr_set_abort(S);
+        break;
+      }
+      const uint8_t* raw = rawb + (it & 1) * CF::kRawBytes;
+      uint8_t* stage = stages + st * kPrStageBytes;
+#pragma unroll 4
+      for (int u = 0; u < (kF8 ? (kTile * 32) / (32 * CF::kDequantWarps + (kF8 ? 0 : 1)) : 0); ++u) {
+        const int ci = dt + u * 32 * CF::kDequantWarps;
+        const int row = ci >> 5, k = ci & 31;   // chunk k = latent 8k .. 8k + 7 of this CTA's 256
+        const uint2 codes = *reinterpret_cast<const uint2*>(raw + row * 256 + 8 * k);
+        const float sc = reinterpret_cast<const float*>(raw + CF::kRawCodes + row * 16)[2 * rank + (k >> 4)];
+        const uint32_t cw[2] = {codes.x, codes.y};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint16_t pair = static_cast<uint16_t>(cw[i >> 1] >> (16 * (i & 1)));
+          uint32_t h2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+          const float2 v = add_f16x2_f32(h2, 0u);
+          o[i] = tc::pack_bf16(v.x * sc, v.y * sc);
+        }
+        *reinterpret_cast<uint4*>(stage + (k >> 3) * kPrBox + row * 128 + (((k & 7) ^ (row & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&S->raw_empty[it & 1]);
+        tc::mbar_arrive_cluster(ready0 + 8u * st);
+      }
     }
   } else {
     // ---------------------------------------------------------------- softmax + segment epilogue

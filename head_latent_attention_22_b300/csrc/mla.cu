@@ -263,13 +263,8 @@ TcPlan tc_plan(int batch) {
   return p;
 }
 
-template <bool kF8>
-constexpr size_t attend_smem() {
-  return 1024 + tcd::AttendLayout<kF8>::kXbuf + 2 * tcd::kXbufBytes + sizeof(tcd::AttendSmem);
-}
-static_assert(attend_smem<false>() <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
-static_assert(tcd::kPrSmem <= 232448, "pair attend kernel shared memory exceeds the 227 KB a CTA may use");
-static_assert(attend_smem<true>() <= 232448, "attend kernel (FP8 cache) shared memory exceeds 227 KB");
+static_assert(tcd::PairCfg<false>::kSmem <= 232448, "attend kernel shared memory exceeds the 227 KB a CTA may use");
+static_assert(tcd::PairCfg<true>::kSmem <= 232448, "attend kernel (FP8 cache) shared memory exceeds 227 KB");
 constexpr size_t kUvSmem = 1024 + tcd::kUvSmem;
 size_t absorb_smem(int nb) { return 1024 + 4 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
 
@@ -314,11 +309,11 @@ mla_status tc_device_setup(int* clusters) {
     if ((e = cudaFuncSetAttribute(tcd::uv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kUvSmem))) != cudaSuccess)
       return cuda_fail(e, "uv smem attribute");
-    mla_status s = cluster_count(reinterpret_cast<const void*>(tcd::attend_pair_kernel), tcd::kPrThreads,
-                                 tcd::kPrSmem, &st.clusters[0]);
+    mla_status s = cluster_count(reinterpret_cast<const void*>(tcd::attend_pair_kernel<false>),
+                                 tcd::PairCfg<false>::kThreads, tcd::PairCfg<false>::kSmem, &st.clusters[0]);
     if (s != MLA_OK) return s;
-    if ((s = cluster_count(reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>), tcd::kAttendThreads,
-                           attend_smem<true>(), &st.clusters[1])) != MLA_OK)
+    if ((s = cluster_count(reinterpret_cast<const void*>(tcd::attend_pair_kernel<true>), tcd::PairCfg<true>::kThreads,
+                           tcd::PairCfg<true>::kSmem, &st.clusters[1])) != MLA_OK)
       return s;
     st.ready = true;
   }
@@ -365,13 +360,13 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
-  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo, m_q, m_qr, m_rope32;
+  CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo, m_q, m_qr;
   uint16_t* o_hi = reinterpret_cast<uint16_t*>(ws + p.off_hi);
   uint16_t* o_lo = reinterpret_cast<uint16_t*>(ws + p.off_lo);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle SW64 = CU_TENSOR_MAP_SWIZZLE_64B;
   bool maps_ok;
-  int rope_x;
   if (f8) {
     // FP8 row: 512 E4M3 codes, 4 fp32 block scales, 64 bf16 rope values (656 bytes)
     const uint64_t rb = tcd::kDc + 4 * (tcd::kDc / 128) + 2 * tcd::kDr;
@@ -380,25 +375,21 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
     const uint8_t* rope_base = static_cast<const uint8_t*>(pool) + tcd::kDc + 4 * (tcd::kDc / 128);
     maps_ok = make_map_2d(&m_lat, pool, U8, rb, static_cast<uint64_t>(pool_rows), rb, 256, tcd::kTile, NS) &&
               make_map_2d(&m_scale, pool, U8, rb, static_cast<uint64_t>(pool_rows), rb, 16, tcd::kTile, NS) &&
-              make_map_2d(&m_rope, rope_base, BF, tcd::kDr, static_cast<uint64_t>(pool_rows), rb, 64, tcd::kTile, SW);
-    rope_x = 0;
+              make_map_2d(&m_rope, rope_base, BF, tcd::kDr, static_cast<uint64_t>(pool_rows), rb, 32, tcd::kTile,
+                          SW64);
   } else {
     maps_ok = make_map_2d(&m_lat, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, tcd::kTile,
-                          SW);
-    m_scale = m_lat;
-    m_rope = m_lat;
-    rope_x = tcd::kDc;
-    // the pair kernel reads Q_lat row-major [B * 128, 576] in boxes of 16 heads x 64 values (latent) and
-    // 16 heads x 32 values (rope), and the pool's rope columns in boxes of 64 rows x 32 values
-    const CUtensorMapSwizzle SW64 = CU_TENSOR_MAP_SWIZZLE_64B;
-    maps_ok = maps_ok &&
-              make_map_2d(&m_q, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 64, 16,
                           SW) &&
-              make_map_2d(&m_qr, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 32, 16,
-                          SW64) &&
-              make_map_2d(&m_rope32, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 32,
+              make_map_2d(&m_rope, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 32,
                           tcd::kTile, SW64);
+    m_scale = m_lat;   // unused with a bf16 pool
   }
+  // Q_lat row-major [B * 128, 576], read in boxes of 16 heads x 64 values (latent) and 16 heads x 32 (rope)
+  maps_ok = maps_ok &&
+            make_map_2d(&m_q, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 64, 16,
+                        SW) &&
+            make_map_2d(&m_qr, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 32, 16,
+                        SW64);
   if (!maps_ok ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
       !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
@@ -419,7 +410,6 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   aa.nb = p.nb;
   aa.max_seq_len = max_seq_len;
   aa.ncl = ncl;
-  aa.row_major = f8 ? 0 : 1;
 
   tcd::AttendArgs ta{};
   ta.q_lat = q_lat;
@@ -431,7 +421,6 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   ta.batch = batch;
   ta.max_pages = max_pages;
   ta.page_size = c->page_size;
-  ta.rope_x = rope_x;
   ta.scale_log2 = softmax_scale(c) * 1.4426950408889634f;
 
   tcd::MergeArgs ma{};
@@ -453,15 +442,13 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  absorb_smem(p.nb), st, absorb_args);
   if (s != MLA_OK) return s;
   stage_mark(1, st);
-  if (f8) {
-    void* attend_args[] = {&m_lat, &m_scale, &m_rope, &ta};
-    s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_tc_kernel<true>), dim3(2 * ncl),
-                   dim3(tcd::kAttendThreads), attend_smem<true>(), st, attend_args);
-  } else {
-    void* attend_args[] = {&m_lat, &m_rope32, &m_q, &m_qr, &ta};
-    s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_pair_kernel), dim3(2 * ncl), dim3(tcd::kPrThreads),
-                   tcd::kPrSmem, st, attend_args);
-  }
+  void* attend_args[] = {&m_lat, &m_rope, &m_q, &m_qr, &m_scale, &ta};
+  if (f8)
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_pair_kernel<true>), dim3(2 * ncl),
+                   dim3(tcd::PairCfg<true>::kThreads), tcd::PairCfg<true>::kSmem, st, attend_args);
+  else
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::attend_pair_kernel<false>), dim3(2 * ncl),
+                   dim3(tcd::PairCfg<false>::kThreads), tcd::PairCfg<false>::kSmem, st, attend_args);
   if (s != MLA_OK) return s;
   stage_mark(2, st);
   void* merge_args[] = {&ma};

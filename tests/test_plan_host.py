@@ -4,7 +4,7 @@ The decode gives cluster c of nc the tiles [share_begin(c), share_begin(c+1)) of
 and finds the owner of a tile with share_owner. A host program built with nvcc from the
 kernel header checks, for many (T, nc), that the shares tile [0, T) in order and that
 share_owner agrees with a brute-force search; and that the two workspace index maps
-(chunk-major Q_lat and partial O) are bijections onto their arrays.
+(row-major Q_lat and chunk-major partial O) are bijections onto their arrays.
 """
 import os
 import shutil
@@ -41,11 +41,10 @@ int main() {
   }
   // index maps: every element of the arrays is hit exactly once
   const int B = 3, slots = 5;
-  std::vector<int> q(static_cast<size_t>(B) * kQChunks * kH * 8, 0), o(static_cast<size_t>(slots) * kOChunks * kH * 4, 0);
+  std::vector<int> q(static_cast<size_t>(B) * kH * kRow, 0), o(static_cast<size_t>(slots) * kOChunks * kH * 4, 0);
   for (int b = 0; b < B; ++b)
-    for (int c = 0; c < kQChunks; ++c)
-      for (int h = 0; h < kH; ++h)
-        for (int e = 0; e < 8; ++e) q.at(qlat_index(b, c, h) + e)++;
+    for (int h = 0; h < kH; ++h)
+      for (int k = 0; k < kRow; ++k) q.at(qlat_row_index(b, h, k))++;
   for (int s = 0; s < slots; ++s)
     for (int c = 0; c < kOChunks; ++c)
       for (int h = 0; h < kH; ++h)
