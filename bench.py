@@ -153,12 +153,13 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str):
-    """dram bytes per launch of `kernel` from the committed ncu summary, if it matches this source."""
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, if it was
+    captured on this source (same digest of the kernel sources); None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        rec = json.load(open(path)).get(kernel)
-    except (OSError, ValueError):
+        rec = json.load(open(path)).get(kernel, {}).get(workload)
+    except (OSError, ValueError, AttributeError):
         return None
     if not rec or rec.get("source_digest") != source_digest():
         return None
@@ -236,6 +237,7 @@ def run_gpu(args, rank, world, local):
     with ClockSampler(local) as clocks:
         for k in range(args.steps):
             flush_l2()
+            torch.cuda._sleep(2_000_000)   # the step's launches are all queued before its first event fires
             ev[k][0].record(stream)
             step(args.warmup + k)
             ev[k][1].record(stream)
@@ -247,11 +249,14 @@ def run_gpu(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = job_value(world, tokens, args.steps, total_ms / 1e3)
 
-    # per-kernel durations (separate pass, same steps, events between the kernels)
+    # per-kernel durations (separate pass, same steps, events between the kernels). A GPU-side
+    # sleep ahead of each step lets the host enqueue all of the step's launches and events before
+    # the first event fires, so an interval holds its kernel's GPU time and no host enqueue gap.
     names = M.decode_stage_names(cfg)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush_l2()
+        torch.cuda._sleep(2_000_000)
         M.set_stage_events(kev[k])
         step(args.warmup + k)
     M.set_stage_events(None)
@@ -277,7 +282,7 @@ def run_gpu(args, rank, world, local):
                 "achieved": round(ach_tf if tensor_bound else ach_gbs, 1),
                 "peak": tf_burst if tensor_bound else hbm, "unit": "TFLOP/s" if tensor_bound else "GB/s",
                 "frac": round(ach_tf / tf_burst if tensor_bound else ach_gbs / hbm, 4),
-                "traffic": committed_traffic(dom), "kernel": dom,
+                "traffic": committed_traffic(dom, shape.name), "kernel": dom,
                 "kernel_ms": round(per_kernel[dom], 5), "algorithmic_bytes": alg_bytes, "algorithmic_flop": alg_flop,
                 "hbm_gbs": round(ach_gbs, 1), "hbm_peak": hbm, "tensor_tflops": round(ach_tf, 1),
                 "tensor_peak": tf_burst,
