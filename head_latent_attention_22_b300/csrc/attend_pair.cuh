@@ -48,6 +48,7 @@ constexpr int kPrSoftmaxWarps = 8;
 constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
 constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
 constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
+constexpr int kPrEarlyBatch = 1024;                 // largest batch whose first tiles load before the plan is read
 
 struct PairSmem {
   uint64_t full[kPrMaxStages];    // this CTA's half of a tile landed (TMA; bf16 cache)
@@ -159,6 +160,85 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
   tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tm = S->tmem_base;
+
+  // The first tiles of this cluster's share go out before the wait on the absorb kernel: the
+  // producer warp derives the share from seq_lens exactly as the plan does (lengths clamped to
+  // [0, max_seq_len], ceil(L / 64) tiles, share [c T / n, (c + 1) T / n)) and requests up to one
+  // ring's worth of tiles. The cache, page table and lengths are complete before the absorb kernel
+  // starts (the decode's contract), so only the queries and the plan wait for it.
+  uint32_t n_pre = 0;
+  int64_t pre_T = 0, pre_t0 = 0;
+  const uint64_t policy = tc::policy_evict_first();
+  auto issue_tile = [&](uint32_t it, int32_t y) {   // lane 0 of the producer warp; slots free for it < ring
+    const int st = it % kPrStages;
+    if (kF8) {
+      uint8_t* raw = rawb + (it & 1) * CF::kRawBytes;
+      uint64_t* bar = &S->raw_full[it & 1];
+      tc::mbar_arrive_expect_tx(bar, CF::kRawBytes + kPrRopeBox);
+      tc::tma_load_2d_hint(raw, &map_lat, static_cast<int>(rank) * 256, y, bar, policy);
+      tc::tma_load_2d_hint(raw + CF::kRawCodes, &map_scale, kDc, y, bar, policy);
+      tc::tma_load_2d_hint(stages + st * kPrStageBytes + 4 * kPrBox, &map_rope, 32 * static_cast<int>(rank), y, bar,
+                           policy);
+    } else {
+      uint8_t* dst = stages + st * kPrStageBytes;
+      tc::mbar_arrive_expect_tx(&S->full[st], kPrStageBytes);
+      for (int k = 0; k < 4; ++k)
+        tc::tma_load_2d_hint(dst + k * kPrBox, &map_lat, static_cast<int>(rank) * 256 + 64 * k, y, &S->full[st],
+                             policy);
+      tc::tma_load_2d_hint(dst + 4 * kPrBox, &map_rope, kDc + 32 * static_cast<int>(rank), y, &S->full[st], policy);
+    }
+  };
+  // pool row of tile j of sequence b (or a row outside the pool, which loads zeros, for a bad page id)
+  auto tile_row = [&](int b, int j) -> int32_t {
+    const int64_t tok = static_cast<int64_t>(j) * kTile;
+    const int pg = static_cast<int>(tok / a.page_size);
+    int64_t page = -1;
+    if (pg < a.max_pages)
+      page = a.block_table ? a.block_table[static_cast<int64_t>(b) * a.max_pages + pg]
+                           : static_cast<int64_t>(b) * a.max_pages + pg;
+    if (page < 0 || page >= a.num_pages) {
+      flag_error(ERR_BIT_BOUNDS);
+      return -2 * kTile;
+    }
+    return static_cast<int32_t>(page * a.page_size + tok % a.page_size);
+  };
+  if (warp == 0 && a.batch <= kPrEarlyBatch) {
+    auto tiles_of = [&](int bb) -> int {
+      if (bb >= a.batch) return 0;
+      int L = a.seq_lens[bb];
+      L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
+      return (L + kTile - 1) / kTile;
+    };
+    for (int base = 0; base < a.batch; base += 32) {
+      int n = tiles_of(base + lane);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+      pre_T += n;
+    }
+    pre_t0 = share_begin(cl, pre_T, ncl);
+    const int64_t t1 = share_begin(cl + 1, pre_T, ncl);
+    const int ring = kF8 ? CF::kRaw : kPrStages;
+    const int want = static_cast<int>(min(static_cast<int64_t>(ring), t1 - pre_t0));
+    // walk the sequences to tile pre_t0 and request the next `want` tiles
+    int64_t acc = 0;
+    int b = 0;
+    while (want > 0 && b < a.batch) {
+      const int n = tiles_of(b);
+      if (acc + n > pre_t0) break;
+      acc += n;
+      ++b;
+    }
+    int j = static_cast<int>(pre_t0 - acc);
+    for (int k = 0; k < want && b < a.batch; ++k) {
+      while (b < a.batch && j >= tiles_of(b)) { j = 0; ++b; }
+      if (b >= a.batch) break;
+      const int32_t y = tile_row(b, j);
+      if (lane == 0) issue_tile(n_pre, y);
+      ++n_pre;
+      ++j;
+    }
+  }
+
   // everything below reads what the absorb kernel wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t* cum = a.plan.cum;
@@ -166,63 +246,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
 
   if (warp == 0) {
     // ---------------------------------------------------------------- cache tiles (both CTAs: own half)
-    const uint64_t policy = tc::policy_evict_first();
     SegIter si = seg_begin(a.plan, a.batch, cl, ncl);
     int b, j0, j1;
     uint32_t it = 0;
     bool ok = true;
+    if (n_pre > 0 && (pre_T != cum[a.batch] || pre_t0 != a.plan.share_start[cl])) {
+      // the lengths changed after this kernel read them: the decode's contract was broken
+      flag_error(ERR_BIT_BOUNDS);
+      ok = false;
+    }
     while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
       for (int jc = j0; jc < j1 && ok; jc += 32) {
         int32_t y_l = 0;
         const int jl = jc + lane;
-        if (jl < j1) {
-          const int64_t tok = static_cast<int64_t>(jl) * kTile;
-          const int pg = static_cast<int>(tok / a.page_size);
-          int64_t page = -1;
-          if (pg < a.max_pages)
-            page = a.block_table ? a.block_table[static_cast<int64_t>(b) * a.max_pages + pg]
-                                 : static_cast<int64_t>(b) * a.max_pages + pg;
-          if (page < 0 || page >= a.num_pages) {
-            flag_error(ERR_BIT_BOUNDS);
-            y_l = -2 * kTile;  // entirely outside the pool: the copy fills zeros
-          } else {
-            y_l = static_cast<int32_t>(page * a.page_size + tok % a.page_size);
-          }
-        }
+        if (jl < j1) y_l = tile_row(b, jl);
         const int n = min(32, j1 - jc);
         for (int u = 0; u < n; ++u) {
           const int32_t y = __shfl_sync(0xffffffffu, y_l, u);
-          if (lane == 0 && ok) {
+          if (lane == 0 && ok && it >= n_pre) {   // tiles before n_pre went out before the wait
             const int st = it % kPrStages;
             if (it >= kPrStages) ok = tc::mbar_wait(&S->empty[st], ((it / kPrStages) - 1) & 1);
             if (kF8 && ok && it >= 2) ok = tc::mbar_wait(&S->raw_empty[it & 1], ((it / 2) - 1) & 1);
             if (ok && pr_aborted(S)) ok = false;
-            if (ok && kF8) {
-              // codes and scales into the raw ring, the bf16 rope values straight into the stage
-              uint8_t* raw = rawb + (it & 1) * CF::kRawBytes;
-              uint64_t* bar = &S->raw_full[it & 1];
-              tc::mbar_arrive_expect_tx(bar, CF::kRawBytes + kPrRopeBox);
-              tc::tma_load_2d_hint(raw, &map_lat, static_cast<int>(rank) * 256, y, bar, policy);
-              tc::tma_load_2d_hint(raw + CF::kRawCodes, &map_scale, kDc, y, bar, policy);
-              tc::tma_load_2d_hint(stages + st * kPrStageBytes + 4 * kPrBox, &map_rope, 32 * static_cast<int>(rank), y,
-                                   bar, policy);
-            } else if (ok) {
-              uint8_t* dst = stages + st * kPrStageBytes;
-              tc::mbar_arrive_expect_tx(&S->full[st], kPrStageBytes);
-              for (int k = 0; k < 4; ++k)
-                tc::tma_load_2d_hint(dst + k * kPrBox, &map_lat, static_cast<int>(rank) * 256 + 64 * k, y,
-                                     &S->full[st], policy);
-              tc::tma_load_2d_hint(dst + 4 * kPrBox, &map_rope, kDc + 32 * static_cast<int>(rank), y, &S->full[st],
-                                   policy);
-            }
-            if (ok) ++it;
+            if (ok) issue_tile(it, y);   // FP8: codes and scales into the raw ring, rope into the stage
           }
+          if (lane == 0 && ok) ++it;
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
         }
       }
     }
     it = __shfl_sync(0xffffffffu, it, 0);
+    if (it < n_pre) it = n_pre;   // tiles requested before the wait are in flight too
     if (lane == 0) {
       if (!ok) pr_set_abort(S);
       // copies still in flight must land before the CTA exits

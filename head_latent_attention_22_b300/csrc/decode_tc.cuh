@@ -236,6 +236,8 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
 struct AttendArgs {
   const uint16_t* q_lat;      // row-major [B, H, 576], see qlat_row_index
   const int32_t* block_table; // [B, max_pages] (NULL: contiguous, sequence b owns pages b*max_pages ..)
+  const int32_t* seq_lens;    // [B] as given to the decode (read before the plan exists)
+  int max_seq_len;
   Plan plan;
   float* part_o;              // chunk-major (see parto_index) fp32, unnormalised
   float* part_ml;             // [slots, H, 2]: running max (log2 units) and sum

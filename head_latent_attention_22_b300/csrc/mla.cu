@@ -414,6 +414,8 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   tcd::AttendArgs ta{};
   ta.q_lat = q_lat;
   ta.block_table = block_table;
+  ta.seq_lens = seq_lens;
+  ta.max_seq_len = max_seq_len;
   ta.plan = plan;
   ta.part_o = reinterpret_cast<float*>(ws + p.off_o);
   ta.part_ml = reinterpret_cast<float*>(ws + p.off_ml);

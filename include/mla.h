@@ -159,14 +159,20 @@ MLA_API size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, i
  * results are merged by a log-sum-exp combine before W_UV is applied.
  *
  * Kernels: n_heads 128, d_c 512, d_rope 64, d_head 128 with bf16 queries and
- * weights, a bf16 or FP8_E4M3_B128 cache, page_size a multiple of 64 and
- * scale > 0 run on the tensor cores (tcgen05/TMEM/TMA, mla_decode_path() == 1;
- * an FP8 cache is dequantised to bf16 in shared memory before the MMAs);
- * every other valid config runs on CUDA cores. On the tensor-core path the kernels are chained
- * with programmatic dependent launch, and the first one may start reading
- * W_UK before the kernel that precedes mla_decode on `stream` has finished:
- * the weights must not be written by that kernel (every other input is read
- * only after it completes).
+ * weights, a bf16 or FP8_E4M3_B128 cache and page_size a multiple of 64 run
+ * on the tensor cores (tcgen05/TMEM/TMA, mla_decode_path() == 1; an FP8 cache
+ * is dequantised to bf16 in shared memory before the MMAs); every other valid
+ * config runs on CUDA cores. On the tensor-core path the kernels are chained
+ * with programmatic dependent launch:
+ *   - the first one may start reading W_UK before the kernel that precedes
+ *     mla_decode on `stream` has finished, so that kernel must not write the
+ *     weights;
+ *   - the attend kernel reads seq_lens, block_table and the pool as soon as
+ *     the first one has started, so the preceding kernel must have finished
+ *     writing them before it allows dependent launches. An ordinary kernel
+ *     (one that never executes griddepcontrol.launch_dependents) allows them
+ *     only when it exits, and always satisfies this.
+ * q_nope and q_rope are read only after the preceding kernel completes.
  */
 MLA_API mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_rope,
                       const void* w_uk, const void* w_uv, const void* pool, int64_t num_pages,
