@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--workload", default="long_b4", choices=sorted(S.SHAPES))
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget per measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="new tokens decoded per sequence per step (multi-token prediction drafts); 1 = plain decode")
     return ap.parse_args()
 
 
@@ -185,7 +187,10 @@ def run_gpu(args, rank, world, local):
     inp = S.make_inputs(shape)
     cfg = M.MLAConfig.from_shape(shape)
     B_, H = shape.batch, shape.n_heads
-    tokens = int(inp.lengths.sum())
+    q = args.q_len
+    cache_tokens = int(inp.lengths.sum())
+    # tokens attended per step: new token k of sequence b sees its first L_b - (q - 1 - k) rows
+    tokens = int(sum(max(0, int(L) - (q - 1 - k)) for L in inp.lengths for k in range(q)))
     max_len = int(inp.lengths.max())
 
     # resident state: weights, page table, pool filled with every token
@@ -196,17 +201,23 @@ def run_gpu(args, rank, world, local):
     pos_all = torch.from_numpy(inp.positions())
     seq_all = torch.from_numpy(inp.seq_index())
     chunk = 1 << 20
-    for s in range(0, tokens, chunk):
-        e = min(tokens, s + chunk)
+    for s in range(0, cache_tokens, chunk):
+        e = min(cache_tokens, s + chunk)
         M.append(cfg, inp.c_kv_raw[s:e].to(dev), inp.k_rope_raw[s:e].to(dev), pos_all[s:e].to(dev), pool, bt,
                  seq_idx=seq_all[s:e].to(dev))
     torch.cuda.synchronize()
     del pos_all, seq_all
 
-    new_pos = torch.from_numpy((inp.lengths - 1).astype(np.int32)).to(dev)
-    new_seq = torch.arange(B_, dtype=torch.int32, device=dev)
-    out = torch.empty((B_, H, shape.d_head), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(256, M.workspace_size(cfg, B_, max_len)), dtype=torch.uint8, device=dev)
+    # the step's new tokens are each sequence's last q rows (rewritten by the step's append)
+    new_pos = torch.from_numpy(np.array([int(L) - q + k for L in inp.lengths for k in range(q)], np.int32)).to(dev)
+    new_seq = torch.from_numpy(np.repeat(np.arange(B_, dtype=np.int32), q)).to(dev)
+    if q == 1:
+        out = torch.empty((B_, H, shape.d_head), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, M.workspace_size(cfg, B_, max_len)), dtype=torch.uint8, device=dev)
+    else:
+        out = torch.empty((B_, q, H, shape.d_head), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, M.workspace_size_multi(cfg, B_, q, bt.shape[1], max_len)), dtype=torch.uint8,
+                         device=dev)
     flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(64 << 20, dtype=torch.int64, device=dev)
 
@@ -214,16 +225,19 @@ def run_gpu(args, rank, world, local):
         flush_w.zero_()
         flush_r.sum()
     n_steps = args.warmup + args.steps
-    steps = [S.draw_step(inp, k) for k in range(min(n_steps, 8))]
+    steps = [S.draw_step(inp, k) if q == 1 else S.draw_step_multi(inp, k, q) for k in range(min(n_steps, 8))]
     dsteps = [tuple(t.to(dev) for t in (st.q_nope, st.q_rope, st.c_new, st.k_new)) for st in steps]
     stream = torch.cuda.current_stream()
 
-    def step(k):
-        qn, qr, cn, kn = dsteps[k % len(dsteps)]
+    def step(k, tensors=None):
+        qn, qr, cn, kn = dsteps[k % len(dsteps)] if tensors is None else tensors
         M.append(cfg, cn, kn, new_pos, pool, bt, seq_idx=new_seq)
-        M.decode(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        if q == 1:
+            M.decode(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        else:
+            M.decode_multi(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
 
-    launches_per_step = 1 + len(M.decode_stage_names(cfg))
+    launches_per_step = 1 + (q > 1) + len(M.decode_stage_names(cfg))
     for k in range(args.warmup):
         step(k)
         flush_l2()
@@ -266,7 +280,9 @@ def run_gpu(args, rank, world, local):
     dom = max(per_kernel, key=per_kernel.get)
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     row = M.cache_row_bytes(cfg)
-    attend_bytes = tokens * row + B_ * H * (shape.d_c + shape.d_rope) * 2
+    # the cache is read once per step (the q new tokens of a sequence share its pages), the queries
+    # of every new token once
+    attend_bytes = cache_tokens * row + B_ * q * H * (shape.d_c + shape.d_rope) * 2
     attend_flop = tokens * H * FLOP_PER_HEAD_TOKEN
     weight_bytes = 2 * H * shape.d_head * shape.d_c * (2 if shape.io_dtype == "bf16" else 4)
     if dom.startswith("attend"):
@@ -282,15 +298,15 @@ def run_gpu(args, rank, world, local):
                 "achieved": round(ach_tf if tensor_bound else ach_gbs, 1),
                 "peak": tf_burst if tensor_bound else hbm, "unit": "TFLOP/s" if tensor_bound else "GB/s",
                 "frac": round(ach_tf / tf_burst if tensor_bound else ach_gbs / hbm, 4),
-                "traffic": committed_traffic(dom, shape.name), "kernel": dom,
+                "traffic": committed_traffic(dom, shape.name + (f"_q{q}" if q > 1 else "")), "kernel": dom,
                 "kernel_ms": round(per_kernel[dom], 5), "algorithmic_bytes": alg_bytes, "algorithmic_flop": alg_flop,
                 "hbm_gbs": round(ach_gbs, 1), "hbm_peak": hbm, "tensor_tflops": round(ach_tf, 1),
                 "tensor_peak": tf_burst,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind,
                 "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()}}
     # whole-step roofline: the slower of all bytes over HBM and all FLOPs over the tensor peak
-    step_bytes = attend_bytes + weight_bytes + B_ * row
-    step_flop = attend_flop + 4 * B_ * H * shape.d_head * shape.d_c
+    step_bytes = attend_bytes + weight_bytes + B_ * q * row
+    step_flop = attend_flop + 4 * B_ * q * H * shape.d_head * shape.d_c
     t_roof = max(step_bytes / (hbm * 1e9), step_flop / (tf_burst * 1e12))
     roofline["step_frac"] = round(t_roof / (ms_per_step / 1e3), 4)
 
@@ -314,9 +330,16 @@ def run_gpu(args, rank, world, local):
     dv = [dblk[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(srcs[0], offs, nbytes)]
     dv_q_nope, dv_q_rope, dv_c_new, dv_k_new = dv
     dblk.copy_(host[0])
-    graph = M.StepGraph(cfg, c_new=dv_c_new, k_new=dv_k_new, positions=new_pos, seq_idx=new_seq, q_nope=dv_q_nope,
-                        q_rope=dv_q_rope, w_uk=w_uk, w_uv=w_uv, pool=pool, block_table=bt, seq_lens=seq_lens,
-                        max_seq_len=max_len, out=out, workspace=ws)
+    if q == 1:
+        graph = M.StepGraph(cfg, c_new=dv_c_new, k_new=dv_k_new, positions=new_pos, seq_idx=new_seq,
+                            q_nope=dv_q_nope, q_rope=dv_q_rope, w_uk=w_uk, w_uv=w_uv, pool=pool, block_table=bt,
+                            seq_lens=seq_lens, max_seq_len=max_len, out=out, workspace=ws)
+        run_step = graph.replay
+        e2e_path = "M.StepGraph replay (CUDA graph of mla_append + mla_decode); inputs in one pinned block"
+    else:
+        def run_step():
+            step(0, (dv_q_nope, dv_q_rope, dv_c_new, dv_k_new))
+        e2e_path = "eager M.append + M.decode_multi calls; inputs in one pinned block"
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(nbytes)
     d2h = out_host.numel() * out_host.element_size()
@@ -326,7 +349,7 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         dblk.copy_(host[k % len(host)], non_blocking=True)
-        graph.replay()
+        run_step()
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         if k >= args.warmup:
@@ -335,15 +358,16 @@ def run_gpu(args, rank, world, local):
     e2e_s = max_over_ranks(e2e_s, world, dev)
     e2e = {"value": job_value(world, tokens, args.steps, e2e_s), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_s / args.steps, 4),
-           "path": "M.StepGraph replay (CUDA graph of mla_append + mla_decode); inputs in one pinned block"}
+           "path": e2e_path}
 
     res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": shape.io_dtype if shape.cache_dtype != "fp8_e4m3_b128"
            else "bf16+fp8cache", "data": "synthetic (seeded; random-init weights)",
-           "config": {"workload": shape.name, "batch": B_, "seq_len": max_len, "cached_tokens": tokens,
+           "config": {"workload": shape.name, "batch": B_, "seq_len": max_len, "cached_tokens": cache_tokens,
+                      "attended_tokens_per_step": tokens,
                       "n_heads": H, "d_c": shape.d_c, "d_rope": shape.d_rope, "d_head": shape.d_head,
-                      "page_size": shape.page_size, "cache_dtype": shape.cache_dtype,
+                      "page_size": shape.page_size, "cache_dtype": shape.cache_dtype, "q_len": q,
                       "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB memset + 512 MiB read)",
                       "decode_path": "tcgen05" if M.decode_path(cfg) else "cuda-core"},
            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

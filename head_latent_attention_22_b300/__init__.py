@@ -20,7 +20,7 @@ from typing import Optional
 import torch
 
 __all__ = ["MLAConfig", "MLAError", "BF16", "FP32", "FP8_E4M3_B128", "library_path", "cache_row_bytes",
-           "new_pool", "append", "workspace_size", "decode", "check_device_errors", "decode_path",
+           "new_pool", "append", "workspace_size", "workspace_size_multi", "decode", "check_device_errors", "decode_path",
            "decode_stage_names", "set_stage_events", "decode_static_scratch"]
 
 BF16, FP32, FP8_E4M3_B128 = 0, 1, 2
@@ -211,6 +211,11 @@ def rope_query(cfg: MLAConfig, q_rope_raw: torch.Tensor, positions: torch.Tensor
     _check(_load().mla_rope_query(ctypes.byref(cfg.c()), _ptr(q_rope_raw), _ptr(positions), _ptr(out), B,
                                   _stream(stream)))
     return out
+
+
+def workspace_size_multi(cfg: MLAConfig, batch: int, q_len: int, max_pages: int, max_seq_len: int) -> int:
+    """mla_decode_multi_workspace_size (0 for invalid arguments)."""
+    return int(_load().mla_decode_multi_workspace_size(ctypes.byref(cfg.c()), batch, q_len, max_pages, max_seq_len))
 
 
 def workspace_size(cfg: MLAConfig, batch: int, max_seq_len: int) -> int:

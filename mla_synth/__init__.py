@@ -220,6 +220,20 @@ def draw_step(inp: MLAInputs, step: int) -> StepInputs:
                       _normal(gen, (B, s.d_rope), 1.0, dt))
 
 
+def draw_step_multi(inp: MLAInputs, step: int, q_len: int) -> StepInputs:
+    """Seeded inputs of a step that decodes q_len new tokens per sequence (drafted tokens verified
+    together): queries [B, q_len, H, .] and the q_len newest rows [B * q_len, .] of each sequence,
+    sequence-major."""
+    s = inp.shape
+    gen = torch.Generator().manual_seed(2_000_003 * (step + 1) + 7919 * q_len + s.seed)
+    dt = torch_dtype(s.io_dtype)
+    B, H = s.batch, s.n_heads
+    return StepInputs(_normal(gen, (B, q_len, H, s.d_head), 1.0, dt),
+                      _normal(gen, (B, q_len, H, s.d_rope), 1.0, dt),
+                      _normal(gen, (B * q_len, s.d_c), 1.0, dt),
+                      _normal(gen, (B * q_len, s.d_rope), 1.0, dt))
+
+
 def with_step(inp: MLAInputs, st: StepInputs) -> MLAInputs:
     """A copy of `inp` whose queries and newest tokens are those of `st`."""
     last = inp.last_token_index()

@@ -45,6 +45,10 @@ def test_static_scratch_decode_matches_workspace_decode(name, over):
                                 dc.seq_lens, L, out)
         M.check_device_errors()
         T.assert_close(out.cpu().numpy(), ref, shape.cache_dtype, f"{name} call {call}")
+    # and on its own against the fp64 oracle, every output
+    pairs = [(b, i) for b in range(shape.batch) for i in range(shape.n_heads)]
+    want = T.oracle_outputs(inp, pairs).reshape(out.shape)
+    T.assert_close(out.cpu().numpy(), want, shape.cache_dtype, f"{name} vs oracle")
 
 
 def test_static_scratch_refuses_oversized_requests():
