@@ -147,23 +147,31 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- the GPU arm
 
-def source_digest() -> str:
+# the sources a kernel is built from (paths relative to the repository root); a committed ncu
+# figure is used only while these files are unchanged
+KERNEL_SOURCES = {
+    "attend_tc": ["head_latent_attention_22_b300/csrc/attend_pair.cuh", "head_latent_attention_22_b300/csrc/decode_tc.cuh",
+                  "head_latent_attention_22_b300/csrc/tc.cuh", "head_latent_attention_22_b300/csrc/common.cuh"],
+}
+
+
+def source_digest(files) -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "head_latent_attention_22_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, if it was
-    captured on this source (same digest of the kernel sources); None otherwise."""
+    captured on the kernel's present sources (same digest); None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path)).get(kernel, {}).get(workload)
-    except (OSError, ValueError, AttributeError):
+        files = KERNEL_SOURCES[kernel]
+    except (OSError, ValueError, AttributeError, KeyError):
         return None
-    if not rec or rec.get("source_digest") != source_digest():
+    if not rec or rec.get("source_digest") != source_digest(files):
         return None
     return rec.get("dram_bytes_per_launch")
 
