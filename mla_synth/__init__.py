@@ -15,6 +15,9 @@ d_h^R = 64, init std 0.006, hidden 5120). The five workloads are:
   long_b4     B=4,  DSV2 shapes, L = 131072 each (128K context), bf16
   fp8_b32     B=32, DSV2 shapes, L = 8192 each, E4M3 cache with fp32 scale per 128
 
+and, for prefill (every cached row of a prompt is also a query), prefill_b4: four
+DSV2-shaped prompts of 4096 tokens (draw_prefill gives their queries).
+
 Random streams use torch's CPU generator (bf16 values are drawn in fp32 and
 cast by torch), seeded per workload; every array is returned on the CPU.
 """
@@ -81,7 +84,12 @@ SHAPES = {
     # beta = 32 over the 4K pre-training context, logit factor (0.0707 ln s + 1)^2
     "yarn_b4": MLAShape("yarn_b4", 4, 128, 512, 64, 128, 64, BF16, BF16, DSV2_W_STD,
                         1.0 / math.sqrt(192), 5, lengths=(131072,) * 4, yarn_factor=40.0),
+    # prefill: 4 prompts of 4096 tokens, each token a query over its prefix
+    "prefill_b4": MLAShape("prefill_b4", 4, 128, 512, 64, 128, 64, BF16, BF16, DSV2_W_STD,
+                           1.0 / math.sqrt(192), 6, lengths=(4096,) * 4),
 }
+
+PREFILL_SHAPES = ("prefill_b4",)
 
 
 def shape_with(base: str, **kw) -> MLAShape:
@@ -243,3 +251,29 @@ def with_step(inp: MLAInputs, st: StepInputs) -> MLAInputs:
     k_rope_raw[last] = st.k_new
     return dataclasses.replace(inp, q_nope=st.q_nope, q_rope=st.q_rope,
                                c_kv_raw=c_kv_raw, k_rope_raw=k_rope_raw)
+
+
+@dataclasses.dataclass
+class PrefillInputs:
+    """Queries of a prefill: the last n_new[b] cached rows of sequence b are its new tokens, and
+    new token k of sequence b is query row q_start[b] + k."""
+
+    q_nope: torch.Tensor   # [T, H, d_h]
+    q_rope: torch.Tensor   # [T, H, d_rope], already rotated
+    n_new: np.ndarray      # int64 [B]
+    q_start: np.ndarray    # int64 [B+1] prefix sums of n_new
+
+
+def draw_prefill(inp: MLAInputs, n_new: Optional[np.ndarray] = None, step: int = 0) -> PrefillInputs:
+    """Seeded queries of a prefill over `inp`'s cache; n_new defaults to whole prompts
+    (every cached row of every sequence is a new token)."""
+    s = inp.shape
+    n = np.asarray(inp.lengths if n_new is None else n_new, dtype=np.int64)
+    assert n.shape == (s.batch,) and (n >= 0).all() and (n <= inp.lengths).all()
+    qs = np.zeros(s.batch + 1, dtype=np.int64)
+    qs[1:] = np.cumsum(n)
+    T = int(qs[-1])
+    gen = torch.Generator().manual_seed(3_000_017 * (step + 1) + s.seed)
+    dt = torch_dtype(s.io_dtype)
+    return PrefillInputs(_normal(gen, (T, s.n_heads, s.d_head), 1.0, dt),
+                         _normal(gen, (T, s.n_heads, s.d_rope), 1.0, dt), n, qs)

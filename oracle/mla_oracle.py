@@ -24,6 +24,9 @@ gain and no norm on k^R, RoPE base 10000 with RoFormer's interleaved pairs
 (2m, 2m+1), 0-based positions, the cache modelled in its storage format) are
 the plainest ones the surrounding prose supports.
 
+Prefill (`prefill`) is the same attention with every new token of a prompt
+as a query, causal over the rows up to its position, in the explicit form.
+
 Two decode forms are given. `decode_explicit` materialises every per-head key
 and value, exactly as 2.1.1 + 2.1.2 state attention. `decode_absorbed` uses
 the absorption identity of 2.1.2 (W_UK folded into the query, W_UV applied
@@ -314,6 +317,49 @@ def decode_multi(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_se
         cs = [c[:max(0, len(c) - drop)] for c in c_seqs]
         ks = [r[:max(0, len(r) - drop)] for r in kr_seqs]
         out[:, k] = decode(q_nope[:, k], q_rope[:, k], w_uk, w_uv, cs, ks, scale, form)
+    return out
+
+
+def prefill(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_seqs: Sequence[np.ndarray],
+            n_new: Sequence[int], scale: float, heads: Optional[Sequence[int]] = None,
+            rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Prefill (or one chunk of a prompt) in the non-absorbed form of section 2.1.2: out [T, H, d_h].
+
+    Sequence b caches L_b = len(c_seqs[b]) rows; its last n_b = n_new[b] rows are its new tokens,
+    query rows q_start[b] .. q_start[b] + n_b - 1 of q_nope [T, H, d_h] and q_rope [T, H, d_r]
+    (q_start = prefix sums of n_new). New token k sits at position p = L_b - n_b + k and attends
+    causally (section 2.1.1) to rows 0 .. p, with the per-head keys [W_UK_i c_j ; kR_j] and values
+    W_UV_i c_j materialised (sections 2.1.2-2.1.3). Only the requested heads and query rows are
+    computed; the rest is NaN.
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    w_uk = np.asarray(w_uk, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    T, H, d_h = q_nope.shape
+    n_new = [int(n) for n in n_new]
+    q_start = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int64)
+    assert q_start[-1] == T
+    want = np.zeros(T, dtype=bool)
+    want[list(range(T)) if rows is None else list(rows)] = True
+    out = np.full((T, H, d_h), np.nan)
+    for b, n in enumerate(n_new):
+        mine = [k for k in range(n) if want[q_start[b] + k]]
+        if not mine:
+            continue
+        c = np.asarray(c_seqs[b], np.float64)
+        kr = np.asarray(kr_seqs[b], np.float64)
+        L = len(c)
+        assert 0 <= n <= L
+        for i in (range(H) if heads is None else heads):
+            k_i = np.concatenate([c @ w_uk[i].T, kr], axis=1)     # [L, d_h + d_r]
+            v_i = c @ w_uv[i].T                                    # [L, d_h]
+            for k in mine:
+                r = q_start[b] + k
+                p = L - n + k
+                q = np.concatenate([q_nope[r, i], q_rope[r, i]])
+                a = softmax_probs(scale * (k_i[:p + 1] @ q))
+                out[r, i] = a @ v_i[:p + 1]
     return out
 
 

@@ -496,3 +496,65 @@ def test_prefill_is_the_multi_token_decode_over_every_position():
                                atol=1e-12)
     # the first token attends only to itself: its value
     np.testing.assert_allclose(a[0, 0], np.einsum("hdk,k->hd", w_uv, c[0]), rtol=1e-12, atol=1e-13)
+
+
+def _prefill_case(seed, lens, n_new, H=3, d_h=4, d_c=6, d_r=2):
+    rng = np.random.default_rng(seed)
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    cs = [rng.standard_normal((L, d_c)) for L in lens]
+    ks = [rng.standard_normal((L, d_r)) for L in lens]
+    T = int(sum(n_new))
+    qn, qr = rng.standard_normal((T, H, d_h)), rng.standard_normal((T, H, d_r))
+    return qn, qr, w_uk, w_uv, cs, ks
+
+
+def test_prefill_is_causal_attention_with_ragged_new_tokens():
+    # whole prompts, a chunk after a cached prefix, a sequence with no new token
+    lens, n_new = [7, 10, 4, 1], [7, 3, 0, 1]
+    qn, qr, w_uk, w_uv, cs, ks = _prefill_case(11, lens, n_new)
+    got = O.prefill(qn, qr, w_uk, w_uv, cs, ks, n_new, 0.37)
+    r = 0
+    for b, (L, n) in enumerate(zip(lens, n_new)):
+        if n:
+            want = _causal_brute_force(qn[r:r + n], qr[r:r + n], w_uk, w_uv, cs[b], ks[b], 0.37, n)
+            np.testing.assert_allclose(got[r:r + n], want, rtol=1e-11, atol=1e-12)
+        r += n
+    assert r == len(got)
+
+
+def test_prefill_chunks_compose_and_end_in_the_plain_decode():
+    L, a = 11, 4
+    qn, qr, w_uk, w_uv, cs, ks = _prefill_case(12, [L], [L])
+    whole = O.prefill(qn, qr, w_uk, w_uv, cs, ks, [L], 0.29)
+    # the first a tokens as a prompt of their own, then the rest as a chunk over the whole cache
+    first = O.prefill(qn[:a], qr[:a], w_uk, w_uv, [cs[0][:a]], [ks[0][:a]], [a], 0.29)
+    rest = O.prefill(qn[a:], qr[a:], w_uk, w_uv, cs, ks, [L - a], 0.29)
+    np.testing.assert_allclose(np.concatenate([first, rest]), whole, rtol=1e-12, atol=1e-13)
+    # the last prompt token sees every row: the absorbed single-token decode
+    dec = O.decode(qn[-1:], qr[-1:], w_uk, w_uv, cs, ks, 0.29)
+    np.testing.assert_allclose(whole[-1], dec[0], rtol=1e-10, atol=1e-12)
+    # the first prompt token sees only itself: its value
+    np.testing.assert_allclose(whole[0], np.einsum("hdk,k->hd", w_uv, cs[0][0]), rtol=1e-12, atol=1e-13)
+
+
+def test_prefill_equals_the_absorbed_multi_token_decode():
+    lens, q = [6, 9], 3
+    qn, qr, w_uk, w_uv, cs, ks = _prefill_case(13, lens, [q, q])
+    got = O.prefill(qn, qr, w_uk, w_uv, cs, ks, [q, q], 0.5)
+    H, d_h = w_uk.shape[:2]
+    multi = O.decode_multi(qn.reshape(2, q, H, d_h), qr.reshape(2, q, H, -1), w_uk, w_uv, cs, ks, 0.5,
+                           form="absorbed")
+    np.testing.assert_allclose(got, multi.reshape(2 * q, H, d_h), rtol=1e-10, atol=1e-12)
+
+
+def test_prefill_subset_matches_the_full_result():
+    lens, n_new = [8, 5], [8, 2]
+    qn, qr, w_uk, w_uv, cs, ks = _prefill_case(14, lens, n_new)
+    full = O.prefill(qn, qr, w_uk, w_uv, cs, ks, n_new, 0.4)
+    part = O.prefill(qn, qr, w_uk, w_uv, cs, ks, n_new, 0.4, heads=[1], rows=[0, 7, 9])
+    for r in range(len(full)):
+        for i in range(full.shape[1]):
+            if i == 1 and r in (0, 7, 9):
+                np.testing.assert_array_equal(part[r, i], full[r, i])
+            else:
+                assert np.isnan(part[r, i]).all()
