@@ -21,7 +21,7 @@ import torch
 
 __all__ = ["MLAConfig", "MLAError", "BF16", "FP32", "FP8_E4M3_B128", "library_path", "cache_row_bytes",
            "new_pool", "append", "workspace_size", "workspace_size_multi", "decode", "check_device_errors", "decode_path",
-           "decode_stage_names", "set_stage_events", "decode_static_scratch"]
+           "decode_stage_names", "set_stage_events", "decode_static_scratch", "prefill", "prefill_workspace_size"]
 
 BF16, FP32, FP8_E4M3_B128 = 0, 1, 2
 _DTYPE_NAMES = {"bf16": BF16, "fp32": FP32, "fp8_e4m3_b128": FP8_E4M3_B128}
@@ -121,6 +121,8 @@ def _load():
         "mla_rope_query": (I32, [CFG, P, P, P, I32, P]),
         "mla_decode_multi_workspace_size": (SZ, [CFG, I32, I32, I32, I32]),
         "mla_decode_multi": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, I32, P, P, SZ, P]),
+        "mla_prefill_workspace_size": (SZ, [CFG, I32, I32]),
+        "mla_prefill": (I32, [CFG, P, P, P, P, P, I64, P, P, P, I32, I32, I32, I32, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -303,6 +305,55 @@ def decode_multi(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_u
     _check(_load().mla_decode_multi(ctypes.byref(cfg.c()), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(w_uv),
                                     _ptr(pool), pool.shape[0], _ptr(block_table), _ptr(seq_lens), B, q, max_pages,
                                     max_seq_len, _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def prefill_workspace_size(cfg: MLAConfig, batch: int, max_seq_len: int) -> int:
+    """mla_prefill_workspace_size (0 when cfg has no prefill kernels)."""
+    return int(_load().mla_prefill_workspace_size(ctypes.byref(cfg.c()), batch, max_seq_len))
+
+
+def prefill(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: torch.Tensor, w_uv: torch.Tensor,
+            pool: torch.Tensor, block_table: Optional[torch.Tensor], seq_lens: torch.Tensor, q_start: torch.Tensor,
+            max_seq_len: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            max_pages: Optional[int] = None, stream=None) -> torch.Tensor:
+    """mla_prefill: every new token of each sequence attends causally to its prefix -> [T, H, d_head] fp32.
+
+    q_nope [T, H, d_head], q_rope [T, H, d_rope] (rotated); q_start [B + 1] int32: the new tokens of
+    sequence b are query rows q_start[b] .. q_start[b+1]-1 and the last rows of its seq_lens[b]
+    cached rows."""
+    dt = cfg.io_torch_dtype
+    _need(q_nope, "q_nope", dt, 3)
+    _need(q_rope, "q_rope", dt, 3)
+    _need(w_uk, "w_uk", dt, 3)
+    _need(w_uv, "w_uv", dt, 3)
+    _need(pool, "pool", torch.uint8)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(q_start, "q_start", torch.int32, 1)
+    T, H = q_nope.shape[0], cfg.n_heads
+    B = seq_lens.shape[0]
+    if q_nope.shape != (T, H, cfg.d_head) or q_rope.shape != (T, H, cfg.d_rope):
+        raise ValueError("query shapes do not match cfg")
+    if q_start.shape[0] != B + 1:
+        raise ValueError("q_start must have batch + 1 entries")
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        max_pages = block_table.shape[1]
+    if max_pages is None:
+        raise ValueError("max_pages is needed without a block table")
+    if out is None:
+        out = torch.empty((T, H, cfg.d_head), dtype=torch.float32, device=q_nope.device)
+    _need(out, "out", torch.float32, 3)
+    need = prefill_workspace_size(cfg, B, max_seq_len)
+    if need == 0:
+        raise MLAError(2, "no prefill kernels for this config (or invalid sizes)")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
+    _need(workspace, "workspace", torch.uint8)
+    _check(_load().mla_prefill(ctypes.byref(cfg.c()), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(w_uv),
+                               _ptr(pool), pool.shape[0], _ptr(block_table), _ptr(seq_lens), _ptr(q_start), B,
+                               max_pages, max_seq_len, T, _ptr(out), _ptr(workspace), workspace.numel(),
+                               _stream(stream)))
     return out
 
 

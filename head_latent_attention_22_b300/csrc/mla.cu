@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "decode_simt.cuh"
 #include "decode_tc.cuh"
+#include "prefill.cuh"
 #include "tmap.cuh"
 
 namespace mla {
@@ -466,6 +467,121 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   return MLA_OK;
 }
 
+// ------------------------------------------------------------------ prefill (tensor cores)
+// Workspace: K_nope (bf16) and V (fp16) of every row of every sequence, [B * lpad, 128 * 128] each, with
+// lpad = max_seq_len rounded up to whole 128-row tiles.
+struct PfPlan {
+  int lpad;
+  size_t off_k, off_v, bytes;
+};
+
+PfPlan pf_plan(int batch, int max_seq_len) {
+  PfPlan p{};
+  const int L = max_seq_len > 0 ? max_seq_len : 1;
+  p.lpad = (L + tcd::kPfRows - 1) / tcd::kPfRows * tcd::kPfRows;
+  const size_t kv = static_cast<size_t>(batch) * p.lpad * tcd::kH * tcd::kDh * 2;
+  p.off_k = 0;
+  p.off_v = align_up(kv, 256);
+  p.bytes = p.off_v + align_up(kv, 256);
+  return p;
+}
+
+static_assert(tcd::kKvSmem <= 232448, "kv_up kernel shared memory exceeds the 227 KB a CTA may use");
+static_assert(tcd::kPaSmem <= 232448, "prefill attention kernel shared memory exceeds 227 KB");
+
+bool g_pf_ready[64] = {};
+
+mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rope, const void* w_uk, const void* w_uv,
+                      const void* pool, int64_t num_pages, const int32_t* block_table, const int32_t* seq_lens,
+                      const int32_t* q_start, int batch, int max_pages, int max_seq_len, int n_tokens, float* out,
+                      void* workspace, size_t workspace_bytes, cudaStream_t st) {
+  const PfPlan p = pf_plan(batch, max_seq_len);
+  if (workspace_bytes < p.bytes)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, p.bytes);
+  const int64_t pool_rows = num_pages * static_cast<int64_t>(c->page_size);
+  const int64_t kv_rows = static_cast<int64_t>(batch) * p.lpad;
+  if (pool_rows >= (static_cast<int64_t>(1) << 31) || kv_rows >= (static_cast<int64_t>(1) << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "pool or key rows exceed the 2^31 rows a tile coordinate can address");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device %d beyond 64 devices", dev);
+  {
+    std::lock_guard<std::mutex> lock(g_tc_mu);
+    if (!g_pf_ready[dev]) {
+      if ((e = cudaFuncSetAttribute(tcd::kv_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(tcd::kKvSmem))) != cudaSuccess)
+        return cuda_fail(e, "kv_up smem attribute");
+      if ((e = cudaFuncSetAttribute(tcd::prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(tcd::kPaSmem))) != cudaSuccess)
+        return cuda_fail(e, "prefill attention smem attribute");
+      g_pf_ready[dev] = true;
+    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* k_buf = reinterpret_cast<uint16_t*>(ws + p.off_k);
+  uint16_t* v_buf = reinterpret_cast<uint16_t*>(ws + p.off_v);
+  const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint64_t wkv = static_cast<uint64_t>(tcd::kH) * tcd::kDh;
+  CUtensorMap m_lat, m_wuk, m_wuv, m_qn, m_qr, m_k, m_v;
+  if (!make_map_2d(&m_lat, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, 64, SW) ||
+      !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt, SW) ||
+      !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt, SW) ||
+      !make_map_2d(&m_qn, q_nope, BF, wkv, static_cast<uint64_t>(n_tokens), wkv * 2, 64, tcd::kPfRows, SW) ||
+      !make_map_2d(&m_qr, q_rope, BF, static_cast<uint64_t>(tcd::kH) * tcd::kDr, static_cast<uint64_t>(n_tokens),
+                   static_cast<uint64_t>(tcd::kH) * tcd::kDr * 2, 64, tcd::kPfRows, SW) ||
+      !make_map_2d(&m_k, k_buf, BF, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64, tcd::kPfRows, SW) ||
+      !make_map_2d(&m_v, v_buf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64,
+                   tcd::kPfRows, SW))
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled refused a tensor description (or the driver entry point is missing)");
+
+  tcd::KvUpArgs ka{};
+  ka.block_table = block_table;
+  ka.seq_lens = seq_lens;
+  ka.k_buf = k_buf;
+  ka.v_buf = v_buf;
+  ka.num_pages = num_pages;
+  ka.batch = batch;
+  ka.max_pages = max_pages;
+  ka.page_size = c->page_size;
+  ka.max_seq_len = max_seq_len;
+  ka.lpad = p.lpad;
+
+  tcd::PrefillArgs pa{};
+  pa.block_table = block_table;
+  pa.seq_lens = seq_lens;
+  pa.q_start = q_start;
+  pa.out = out;
+  pa.num_pages = num_pages;
+  pa.batch = batch;
+  pa.max_pages = max_pages;
+  pa.page_size = c->page_size;
+  pa.max_seq_len = max_seq_len;
+  pa.lpad = p.lpad;
+  pa.n_tokens = n_tokens;
+  pa.qt_max = p.lpad / tcd::kPfRows;
+  pa.scale_log2 = softmax_scale(c) * 1.4426950408889634f;
+
+  const int sms = current_sm_count();
+  const int64_t items = static_cast<int64_t>(p.lpad / tcd::kPfRows) * batch * tcd::kKvGroups;
+  const int g_kv = static_cast<int>(items < sms ? items : sms);
+  const int64_t units = static_cast<int64_t>(batch) * tcd::kH * pa.qt_max;
+  const int g_pa = static_cast<int>(units < sms ? units : sms);
+  stage_mark(0, st);
+  void* kv_args[] = {&m_lat, &m_wuk, &m_wuv, &ka};
+  mla_status s = launch_pdl(reinterpret_cast<const void*>(tcd::kv_up_kernel), dim3(g_kv), dim3(tcd::kKvThreads),
+                            tcd::kKvSmem, st, kv_args);
+  if (s != MLA_OK) return s;
+  stage_mark(1, st);
+  void* pa_args[] = {&m_qn, &m_qr, &m_k, &m_v, &m_lat, &pa};
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::prefill_attn_kernel), dim3(g_pa), dim3(tcd::kPaThreads),
+                 tcd::kPaSmem, st, pa_args);
+  if (s != MLA_OK) return s;
+  stage_mark(2, st);
+  return MLA_OK;
+}
+
 // ------------------------------------------------------------------ fixed scratch
 // Scratch of mla_decode_static_scratch: one array per device, for callers
 // that cannot allocate. Host code must not use the symbol as an address; the
@@ -650,6 +766,41 @@ mla_status mla_decode_static_scratch(const mla_config* cfg, const void* q_nope, 
   if (s != MLA_OK) return s;
   return mla_decode(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
                     max_seq_len, out, scratch, MLA_STATIC_SCRATCH_BYTES, stream);
+}
+
+size_t mla_prefill_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len) {
+  if (check_config(cfg) != MLA_OK || batch < 1 || max_seq_len < 0 || !tc_supported(cfg) ||
+      cfg->cache_dtype != MLA_DTYPE_BF16)
+    return 0;
+  return pf_plan(batch, max_seq_len).bytes;
+}
+
+mla_status mla_prefill(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
+                       const void* w_uv, const void* pool, int64_t num_pages, const int32_t* block_table,
+                       const int32_t* seq_lens, const int32_t* q_start, int32_t batch, int32_t max_pages,
+                       int32_t max_seq_len, int32_t n_tokens, float* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (!tc_supported(cfg) || cfg->cache_dtype != MLA_DTYPE_BF16)
+    return fail(MLA_ERR_UNSUPPORTED,
+                "prefill runs the DeepSeek-V2 shape (128 heads, d_c 512, d_rope 64, d_head 128) with bf16 "
+                "queries, weights and cache, and pages of a multiple of 64 tokens");
+  if (batch < 1 || max_pages < 1 || num_pages < 1 || max_seq_len < 0 || n_tokens < 0)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: batch=%d max_pages=%d num_pages=%lld max_seq_len=%d n_tokens=%d",
+                batch, max_pages, static_cast<long long>(num_pages), max_seq_len, n_tokens);
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * cfg->page_size)
+    return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (static_cast<int64_t>(n_tokens) > static_cast<int64_t>(batch) * max_seq_len)
+    return fail(MLA_ERR_INVALID_ARG, "n_tokens %d exceeds batch * max_seq_len", n_tokens);
+  if (n_tokens == 0) return MLA_OK;
+  if (!q_nope || !q_rope || !w_uk || !w_uv || !pool || !seq_lens || !q_start || !out || !workspace)
+    return fail(MLA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(pool) ||
+      !aligned16(out) || !aligned16(workspace))
+    return fail(MLA_ERR_INVALID_ARG, "q_nope, q_rope, w_uk, w_uv, pool, out and workspace must be 16-byte aligned");
+  return prefill_tc(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, q_start, batch,
+                    max_pages, max_seq_len, n_tokens, out, workspace, workspace_bytes, as_stream(stream));
 }
 
 mla_status mla_check_device_errors(void* stream) {

@@ -238,6 +238,48 @@ MLA_API mla_status mla_decode_static_scratch(const mla_config* cfg, const void* 
                                              int32_t max_seq_len, float* out, void* stream);
 
 /*
+ * mla_prefill - attention of whole prompts (or prompt chunks) over the
+ * paged latent cache, in the non-absorbed form of the DeepSeek-V2 report,
+ * section 2.1.2 (per-head keys k_{j,i} = W_UK,i c_j and values
+ * v_{j,i} = W_UV,i c_j materialised from the cached latents) with the
+ * decoupled rope key of section 2.1.3 and causal softmax attention
+ * (section 2.1.1). The new tokens must already be in the cache (mla_append):
+ * sequence b holds seq_lens[b] rows, of which the last
+ * n_b = q_start[b+1] - q_start[b] are its new tokens, at positions
+ * seq_lens[b] - n_b .. seq_lens[b] - 1; new token k attends to rows
+ * 0 .. seq_lens[b] - n_b + k (a full prompt has n_b = seq_lens[b]; a chunk
+ * of a longer prompt attends to the rows cached before it too).
+ *   q_nope [n_tokens, n_heads, d_head] io_dtype, q_rope [n_tokens, n_heads,
+ *            d_rope] (rotated at each token's position, e.g. by mla_rope_query)
+ *   w_uk, w_uv [n_heads, d_head, d_c]
+ *   pool, num_pages, block_table, max_pages: as in mla_append (read only)
+ *   seq_lens [batch] int32 (device), q_start [batch + 1] int32 (device),
+ *            non-decreasing, q_start[0] = 0, q_start[batch] = n_tokens
+ *   max_seq_len  host-side upper bound of seq_lens (sizes the workspace)
+ *   out    [n_tokens, n_heads, d_head] fp32: row q_start[b] + k is new token k
+ *          of sequence b, out = sum_j softmax_j(scale q.k_j) v_j per head
+ *   workspace, workspace_bytes: at least mla_prefill_workspace_size() bytes
+ *          (the per-head keys and values, 2 * batch * ceil(max_seq_len/128)
+ *          * 128 * n_heads * d_head bf16 values)
+ * Supported: the DeepSeek-V2 shape with bf16 queries, weights and cache and
+ * page_size a multiple of 64 (MLA_ERR_UNSUPPORTED otherwise; the workspace
+ * size is then 0). A sequence with n_b < 0, n_b > seq_lens[b] or q_start
+ * outside [0, n_tokens] sets MLA_ERR_BOUNDS and is skipped; a page id outside
+ * the pool for a row the sequence holds sets MLA_ERR_BOUNDS and reads zeros.
+ * Kernels: kv_up (tcgen05 GEMM of the latent rows against [W_UK ; W_UV]) and
+ * prefill_attn (tcgen05 causal attention, P kept in tensor memory), chained
+ * with programmatic dependent launch: the preceding kernel on `stream` must
+ * have finished writing the pool, block_table and seq_lens (an ordinary
+ * kernel always has).
+ */
+MLA_API size_t mla_prefill_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len);
+MLA_API mla_status mla_prefill(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
+                               const void* w_uv, const void* pool, int64_t num_pages, const int32_t* block_table,
+                               const int32_t* seq_lens, const int32_t* q_start, int32_t batch, int32_t max_pages,
+                               int32_t max_seq_len, int32_t n_tokens, float* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
  * Waits for `stream`, then returns and clears the current device's error
  * word: MLA_OK, MLA_ERR_BOUNDS or MLA_ERR_TIMEOUT (timeout wins if both).
  */
