@@ -468,11 +468,11 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
 }
 
 // ------------------------------------------------------------------ prefill (tensor cores)
-// Workspace: K_nope (bf16) and V (fp16) of every row of every sequence, [B * lpad, 128 * 128] each, with
-// lpad = max_seq_len rounded up to whole 128-row tiles.
+// Workspace: K_nope (bf16) and V (fp16) of every row of every sequence, [B * lpad, 128 * 128] each, and
+// the rows' rope keys [B * lpad, 64] bf16, with lpad = max_seq_len rounded up to whole 128-row tiles.
 struct PfPlan {
   int lpad;
-  size_t off_k, off_v, bytes;
+  size_t off_k, off_v, off_kr, bytes;
 };
 
 PfPlan pf_plan(int batch, int max_seq_len) {
@@ -482,7 +482,8 @@ PfPlan pf_plan(int batch, int max_seq_len) {
   const size_t kv = static_cast<size_t>(batch) * p.lpad * tcd::kH * tcd::kDh * 2;
   p.off_k = 0;
   p.off_v = align_up(kv, 256);
-  p.bytes = p.off_v + align_up(kv, 256);
+  p.off_kr = p.off_v + align_up(kv, 256);
+  p.bytes = p.off_kr + align_up(static_cast<size_t>(batch) * p.lpad * tcd::kDr * 2, 256);
   return p;
 }
 
@@ -521,10 +522,11 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint16_t* k_buf = reinterpret_cast<uint16_t*>(ws + p.off_k);
   uint16_t* v_buf = reinterpret_cast<uint16_t*>(ws + p.off_v);
+  uint16_t* kr_buf = reinterpret_cast<uint16_t*>(ws + p.off_kr);
   const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
   const uint64_t wkv = static_cast<uint64_t>(tcd::kH) * tcd::kDh;
-  CUtensorMap m_lat, m_wuk, m_wuv, m_qn, m_qr, m_k, m_v;
+  CUtensorMap m_lat, m_wuk, m_wuv, m_qn, m_qr, m_k, m_v, m_kr;
   if (!make_map_2d(&m_lat, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, 64, SW) ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt, SW) ||
       !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt, SW) ||
@@ -533,14 +535,17 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
                    static_cast<uint64_t>(tcd::kH) * tcd::kDr * 2, 64, tcd::kPfRows, SW) ||
       !make_map_2d(&m_k, k_buf, BF, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64, tcd::kPfRows, SW) ||
       !make_map_2d(&m_v, v_buf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64,
-                   tcd::kPfRows, SW))
+                   tcd::kPfRows, SW) ||
+      !make_map_2d(&m_kr, kr_buf, BF, tcd::kDr, static_cast<uint64_t>(kv_rows), tcd::kDr * 2, 64, tcd::kPfRows, SW))
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled refused a tensor description (or the driver entry point is missing)");
 
   tcd::KvUpArgs ka{};
   ka.block_table = block_table;
   ka.seq_lens = seq_lens;
+  ka.pool = static_cast<const uint16_t*>(pool);
   ka.k_buf = k_buf;
   ka.v_buf = v_buf;
+  ka.kr_buf = kr_buf;
   ka.num_pages = num_pages;
   ka.batch = batch;
   ka.max_pages = max_pages;
@@ -574,7 +579,7 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
                             tcd::kKvSmem, st, kv_args);
   if (s != MLA_OK) return s;
   stage_mark(1, st);
-  void* pa_args[] = {&m_qn, &m_qr, &m_k, &m_v, &m_lat, &pa};
+  void* pa_args[] = {&m_qn, &m_qr, &m_k, &m_v, &m_kr, &pa};
   s = launch_pdl(reinterpret_cast<const void*>(tcd::prefill_attn_kernel), dim3(g_pa), dim3(tcd::kPaThreads),
                  tcd::kPaSmem, st, pa_args);
   if (s != MLA_OK) return s;

@@ -52,6 +52,13 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return r;
 }
 
+// Starts bringing the box at (x, y) of a tensor into L2 (no shared memory, no completion).
+__device__ __forceinline__ void pf_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 constexpr int kPfRows = 128;              // query rows and key rows per tile
 constexpr int kPfBox = kPfRows * 128;     // one TMA box: 128 rows x 64 bf16 (128-byte swizzle) = 16 KB
 constexpr int kPfHalfBox = 64 * 128;      // 64 rows x 64 bf16 = 8 KB
@@ -79,8 +86,10 @@ constexpr size_t kKvSmem = 1024 + kKvABytes + static_cast<size_t>(kKvStages) * k
 struct KvUpArgs {
   const int32_t* block_table;   // [B, max_pages] or NULL (contiguous pages b * max_pages + p)
   const int32_t* seq_lens;      // [B]
+  const uint16_t* pool;         // [num_pages * page_size, 576] bf16
   uint16_t* k_buf;              // [B * lpad, 128 * 128] bf16
   uint16_t* v_buf;              // same, fp16
+  uint16_t* kr_buf;             // [B * lpad, 64] bf16: the shared rope key of every row
   int64_t num_pages;
   int batch, max_pages, page_size, max_seq_len, lpad;
 };
@@ -251,6 +260,24 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int L = clamp_len(a.seq_lens[it.b], a.max_seq_len);
       const bool valid = static_cast<int64_t>(it.r) * kPfRows + row < L;   // rows past L are written as zeros
       const int64_t grow = static_cast<int64_t>(it.b) * a.lpad + static_cast<int64_t>(it.r) * kPfRows + row;
+      if (it.g == 0) {
+        // the row's rope key, copied beside K_nope so that the attention kernel reads whole
+        // 128-row tiles without page lookups (zeros past the sequence's length)
+        uint4 rv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rv[u] = make_uint4(0u, 0u, 0u, 0u);
+        const int64_t tok0 = static_cast<int64_t>(it.r) * kPfRows + (row & ~63);
+        const int32_t prow =
+            valid ? pf_pool_row(a.block_table, a.num_pages, a.max_pages, a.page_size, it.b, tok0, L) : -1;
+        if (prow >= 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.pool + static_cast<int64_t>(prow + (row & 63)) * kRow + kDc);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) rv[u] = src[u];
+        }
+        uint4* dr = reinterpret_cast<uint4*>(a.kr_buf + grow * kDr);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dr[u] = rv[u];
+      }
       for (int t = 0; t < kKvTilesPerItem; ++t, ++d) {
         const uint32_t buf = d & 1;
         bool good = tc::mbar_wait(&S->d_full[buf], (d >> 1) & 1);
@@ -293,11 +320,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ------------------------------------------------------------------ prefill_attn_kernel
-constexpr int kPaStages = 2;
+constexpr int kPaStages = 2;                          // ring depth of key tiles and of value tiles
 constexpr int kPaQBytes = 3 * kPfBox;                 // q_nope (2 boxes) and q_rope (1 box) of 128 rows: 48 KB
-constexpr int kPaKBytes = 3 * kPfBox;                 // k_nope (2 boxes) and the shared rope key (2 x 64 rows)
+constexpr int kPaKBytes = 3 * kPfBox;                 // k_nope (2 boxes) and the shared rope key (1 box)
 constexpr int kPaVBytes = 2 * kPfBox;                 // V: 2 boxes of 128 rows x 64 columns
-constexpr int kPaStageBytes = kPaKBytes + kPaVBytes;  // 80 KB
 constexpr int kPaSoftmaxWarps = 8;
 constexpr int kPaThreads = 32 * (kPaSoftmaxWarps + 2);
 constexpr uint32_t kPaTmS = 0;     // score buffers: columns 0 and 128
@@ -306,7 +332,7 @@ constexpr uint32_t kPaTmO = 384;   // O: 128 columns
 
 struct PaSmem {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kPaStages], v_full[kPaStages], kv_empty[kPaStages];
+  uint64_t k_full[kPaStages], k_empty[kPaStages], v_full[kPaStages], v_empty[kPaStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
   uint64_t drain;
   float red_max[2][2][kPfRows];   // [tile parity][column half][row]
@@ -314,7 +340,8 @@ struct PaSmem {
   uint32_t tmem_base;
   int32_t abort_flag;
 };
-constexpr size_t kPaSmem = 1024 + kPaQBytes + static_cast<size_t>(kPaStages) * kPaStageBytes + sizeof(PaSmem);
+constexpr size_t kPaSmem =
+    1024 + kPaQBytes + static_cast<size_t>(kPaStages) * (kPaKBytes + kPaVBytes) + sizeof(PaSmem);
 
 struct PrefillArgs {
   const int32_t* block_table;
@@ -360,25 +387,27 @@ __device__ __forceinline__ bool pa_aborted(const PaSmem* s) {
 __device__ __forceinline__ void pa_set_abort(PaSmem* s) { *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1; }
 
 // map_qn: q_nope [T, 128 * 128] bf16; map_qr: q_rope [T, 128 * 64]; map_k / map_v: K_nope (bf16) /
-// V (fp16) [B * lpad, 128 * 128]; map_lat: the pool [rows, 576] (boxes of 64 rows; the rope key at column 512).
-// All boxes are 64 columns wide with the 128-byte swizzle; 128 rows except map_lat's 64.
+// V (fp16) [B * lpad, 128 * 128]; map_kr: the rope keys [B * lpad, 64]. All boxes are 128 rows x 64
+// columns with the 128-byte swizzle.
 __global__ void __launch_bounds__(kPaThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap map_qn, const __grid_constant__ CUtensorMap map_qr,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                        const __grid_constant__ CUtensorMap map_lat, PrefillArgs a) {
+                        const __grid_constant__ CUtensorMap map_kr, PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = sm;
-  uint8_t* stages = sm + kPaQBytes;
-  PaSmem* S = reinterpret_cast<PaSmem*>(stages + kPaStages * kPaStageBytes);
+  uint8_t* kst0 = sm + kPaQBytes;                      // key tiles
+  uint8_t* vst0 = kst0 + kPaStages * kPaKBytes;        // value tiles
+  PaSmem* S = reinterpret_cast<PaSmem*>(vst0 + kPaStages * kPaVBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tc::mbar_init(&S->q_full, 1);
     tc::mbar_init(&S->q_empty, 1);
     for (int s = 0; s < kPaStages; ++s) {
       tc::mbar_init(&S->k_full[s], 1);
+      tc::mbar_init(&S->k_empty[s], 1);
       tc::mbar_init(&S->v_full[s], 1);
-      tc::mbar_init(&S->kv_empty[s], 1);
+      tc::mbar_init(&S->v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&S->s_full[s], 1);
@@ -393,7 +422,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     tc::tma_prefetch_map(&map_qr);
     tc::tma_prefetch_map(&map_k);
     tc::tma_prefetch_map(&map_v);
-    tc::tma_prefetch_map(&map_lat);
+    tc::tma_prefetch_map(&map_kr);
   }
   if (warp == kPaSoftmaxWarps + 1) tc::tmem_alloc<512>(&S->tmem_base);
   tc::tc_fence_before();
@@ -406,9 +435,22 @@ __global__ void __launch_bounds__(kPaThreads, 1)
   const int64_t n_units = static_cast<int64_t>(a.batch) * kH * a.qt_max;
   if (warp == kPaSoftmaxWarps) {
     // ------------------------------------------------------------ producer
+    // key tile g goes out as soon as the score MMA of tile g - 2 completed; value tile g - 1 after
+    // it (its PV comes after the softmax of tile g - 1), once the PV of tile g - 3 completed
     if (lane == 0) {
-      uint32_t n = 0, g = 0;   // units and key tiles loaded
+      uint32_t n = 0, g = 0, gv = 0;   // units, key tiles and value tiles loaded
+      int32_t pend_y = 0, pend_x = 0;  // value tile waiting to go out (when gv < g)
       bool ok = true;
+      auto load_v = [&]() -> bool {
+        const int st = gv % kPaStages;
+        if (gv >= kPaStages && !tc::mbar_wait(&S->v_empty[st], ((gv / kPaStages) - 1) & 1)) return false;
+        uint8_t* dst = vst0 + st * kPaVBytes;
+        tc::mbar_arrive_expect_tx(&S->v_full[st], kPaVBytes);
+        tc::tma_load_2d(dst, &map_v, pend_x, pend_y, &S->v_full[st]);
+        tc::tma_load_2d(dst + kPfBox, &map_v, pend_x + 64, pend_y, &S->v_full[st]);
+        ++gv;
+        return true;
+      };
       for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const PaUnit x = pa_unit(a, u);
         if (!x.live) continue;
@@ -419,34 +461,38 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         tc::tma_load_2d(sQ + kPfBox, &map_qn, x.head * kDh + 64, x.q0, &S->q_full);
         tc::tma_load_2d(sQ + 2 * kPfBox, &map_qr, x.head * kDr, x.q0, &S->q_full);
         ++n;
-        const int L = x.p0 + x.n;
+        // the next unit's queries into L2 while this unit runs
+        for (int64_t w = u + gridDim.x; w < n_units; w += gridDim.x) {
+          const PaUnit y = pa_unit(a, w);
+          if (!y.live) continue;
+          pf_prefetch_2d(&map_qn, y.head * kDh, y.q0);
+          pf_prefetch_2d(&map_qn, y.head * kDh + 64, y.q0);
+          pf_prefetch_2d(&map_qr, y.head * kDr, y.q0);
+          break;
+        }
         const int64_t krow0 = static_cast<int64_t>(x.b) * a.lpad;
         for (int j = 0; j < x.nk && ok; ++j, ++g) {
           const int st = g % kPaStages;
-          if (g >= kPaStages) ok = tc::mbar_wait(&S->kv_empty[st], ((g / kPaStages) - 1) & 1);
+          if (g >= kPaStages) ok = tc::mbar_wait(&S->k_empty[st], ((g / kPaStages) - 1) & 1);
           if (!ok) break;
-          uint8_t* kst = stages + st * kPaStageBytes;
+          uint8_t* kst = kst0 + st * kPaKBytes;
           const int32_t yk = static_cast<int32_t>(krow0 + static_cast<int64_t>(j) * kPfRows);
           tc::mbar_arrive_expect_tx(&S->k_full[st], kPaKBytes);
           tc::tma_load_2d(kst, &map_k, x.head * kDh, yk, &S->k_full[st]);
           tc::tma_load_2d(kst + kPfBox, &map_k, x.head * kDh + 64, yk, &S->k_full[st]);
-          for (int h = 0; h < 2; ++h) {
-            const int64_t tok = static_cast<int64_t>(j) * kPfRows + 64 * h;
-            const int32_t yr = pf_pool_row(a.block_table, a.num_pages, a.max_pages, a.page_size, x.b, tok, L);
-            tc::tma_load_2d(kst + 2 * kPfBox + h * kPfHalfBox, &map_lat, kDc, yr, &S->k_full[st]);
-          }
-          tc::mbar_arrive_expect_tx(&S->v_full[st], kPaVBytes);
-          tc::tma_load_2d(kst + kPaKBytes, &map_v, x.head * kDh, yk, &S->v_full[st]);
-          tc::tma_load_2d(kst + kPaKBytes + kPfBox, &map_v, x.head * kDh + 64, yk, &S->v_full[st]);
+          tc::tma_load_2d(kst + 2 * kPfBox, &map_kr, 0, yk, &S->k_full[st]);
+          if (gv < g) ok = load_v();
+          pend_x = x.head * kDh;
+          pend_y = yk;
         }
       }
+      if (ok && gv < g) ok = load_v();
       if (!ok) pa_set_abort(S);
       if (n > 0) tc::mbar_wait(&S->q_full, (n - 1) & 1);
-      const uint32_t first = g > kPaStages ? g - kPaStages : 0;
-      for (uint32_t q = first; q < g; ++q) {
+      for (uint32_t q = g > kPaStages ? g - kPaStages : 0; q < g; ++q)
         tc::mbar_wait(&S->k_full[q % kPaStages], (q / kPaStages) & 1);
+      for (uint32_t q = gv > kPaStages ? gv - kPaStages : 0; q < gv; ++q)
         tc::mbar_wait(&S->v_full[q % kPaStages], (q / kPaStages) & 1);
-      }
     }
   } else if (warp == kPaSoftmaxWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -454,8 +500,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       const uint32_t idesc_s = tc::idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_o = idesc_f16_f32(128, 128, 0, 1);
       const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);         // K-major Q
-      const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), 16, 1024);     // K-major keys, stage 0
-      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(stages + kPaKBytes), kPfBox, 1024);   // MN-major V
+      const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(kst0), 16, 1024);       // K-major keys, stage 0
+      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(vst0), kPfBox, 1024);   // MN-major V, stage 0
       uint32_t n = 0, g = 0;
       bool ok = true;
       // O (+)= P V of key tile gg (P from TMEM, 16 keys per MMA)
@@ -468,10 +514,10 @@ __global__ void __launch_bounds__(kPaThreads, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           tc::mma_ts(tm + kPaTmO, tm + kPaTmP + 64 * s + 8 * k,
-                     vdesc0 + static_cast<uint64_t>(((gg % kPaStages) * kPaStageBytes + 2048 * k) >> 4), idesc_o,
+                     vdesc0 + static_cast<uint64_t>(((gg % kPaStages) * kPaVBytes + 2048 * k) >> 4), idesc_o,
                      (first && k == 0) ? 0u : 1u);
         tc::mma_commit(&S->o_done[s]);
-        tc::mma_commit(&S->kv_empty[gg % kPaStages]);
+        tc::mma_commit(&S->v_empty[gg % kPaStages]);
         return true;
       };
       for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -484,7 +530,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
           if (ok && g >= 2) ok = tc::mbar_wait(&S->s_free[s], ((g - 2) >> 1) & 1);
           if (!ok || pa_aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
-          const uint32_t kst = (g % kPaStages) * kPaStageBytes;
+          const uint32_t kst = (g % kPaStages) * kPaKBytes;
 #pragma unroll
           for (int k = 0; k < 12; ++k) {
             const uint32_t off = (k >> 2) * kPfBox + (k & 3) * 32;
@@ -492,6 +538,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
                        kdesc0 + static_cast<uint64_t>((kst + off) >> 4), idesc_s, k > 0 ? 1u : 0u);
           }
           tc::mma_commit(&S->s_full[s]);
+          tc::mma_commit(&S->k_empty[g % kPaStages]);
           if (j == x.nk - 1) tc::mma_commit(&S->q_empty);
           if (j >= 1) ok = issue_pv(g - 1, j == 1);
         }
@@ -517,22 +564,24 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       if (!x.live) continue;
       const int qp = x.p0 + kPfRows * x.t + row;   // position of this row's token
       float m_used = -INFINITY, l = 0.f;
+      // a wait that runs out stops this warp's waiting for the rest of the unit; the warps vote at
+      // its end and leave together
+      bool alive = true;
       for (int j = 0; j < x.nk; ++j, ++g) {
         const uint32_t s = g & 1;
-        bool good = tc::mbar_wait(&S->s_full[s], (g >> 1) & 1);
-        good = __all_sync(0xffffffffu, good);
+        if (alive) alive = __all_sync(0xffffffffu, tc::mbar_wait(&S->s_full[s], (g >> 1) & 1));
         tc::tc_fence_after();
         float v[64];
         {
-          uint32_t r[32];
-          tc::tmem_ld32(tm + lane_base + kPaTmS + 128 * s + 64 * hc, r);
+          uint32_t r0[32], r1[32];
+          tc::tmem_ld32(tm + lane_base + kPaTmS + 128 * s + 64 * hc, r0);
+          tc::tmem_ld32(tm + lane_base + kPaTmS + 128 * s + 64 * hc + 32, r1);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          tc::tmem_ld32(tm + lane_base + kPaTmS + 128 * s + 64 * hc + 32, r);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) {
+            v[i] = __uint_as_float(r0[i]);
+            v[32 + i] = __uint_as_float(r1[i]);
+          }
         }
         tc::tc_fence_before();
         __syncwarp();
@@ -544,24 +593,22 @@ __global__ void __launch_bounds__(kPaThreads, 1)
           for (int i = 0; i < 64; ++i)
             if (k0 + i > qp) v[i] = -INFINITY;
         }
-        float mx = v[0];
+        float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, v[i]);
-        S->red_max[s][hc][row] = mx;
+        for (int i = 4; i < 64; i += 4)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m4[k] = fmaxf(m4[k], v[i + k]);
+        S->red_max[s][hc][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         tc::named_sync(1 + q4, 64);
-        mx = fmaxf(S->red_max[s][0][row], S->red_max[s][1][row]);
-        const float mt = mx * sl;
-        bool need = false;
+        const float mt = fmaxf(S->red_max[s][0][row], S->red_max[s][1][row]) * sl;
         if (j == 0) {
           m_used = mt;
         } else {
-          need = mt > m_used + static_cast<float>(kRescaleThreshold);
-          // PV of the previous tile must be complete: it reads the P buffer written next and
-          // accumulates into the O rows a rescale touches
-          bool done = tc::mbar_wait(&S->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1);
-          good = good && __all_sync(0xffffffffu, done);
-          tc::tc_fence_after();
+          const bool need = mt > m_used + static_cast<float>(kRescaleThreshold);
           if (__any_sync(0xffffffffu, need)) {
+            // the O rows a rescale touches: the previous tile's PV must have completed
+            if (alive) alive = __all_sync(0xffffffffu, tc::mbar_wait(&S->o_done[s ^ 1u], ((g - 1) >> 1) & 1));
+            tc::tc_fence_after();
             const float f = need ? tc::ex2_approx(m_used - mt) : 1.f;
             if (need) {
               m_used = mt;
@@ -581,48 +628,51 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         {
           const float neg_m = -m_used;
           uint32_t pk[32];
-          float ls = 0.f;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float e0 = tc::ex2_approx(fmaf(v[2 * i], sl, neg_m));
             const float e1 = tc::ex2_approx(fmaf(v[2 * i + 1], sl, neg_m));
-            ls += e0 + e1;
+            ls[i & 3] += e0 + e1;
             pk[i] = pack_f16(e0, e1);
           }
-          l += ls;
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          // this P buffer was last read by the PV of tile g - 2
+          if (g >= 2 && alive) alive = __all_sync(0xffffffffu, tc::mbar_wait(&S->o_done[s], ((g - 2) >> 1) & 1));
+          tc::tc_fence_after();
           tc::tmem_st32(tm + lane_base + kPaTmP + 64 * s + 32 * hc, pk);
           tc::tmem_st_wait();
         }
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&S->p_full[s]);
-        ok = tc::named_sync_and(5, 32 * kPaSoftmaxWarps, good);
-        if (!ok) break;
       }
-      if (!ok) break;
       // ---- epilogue: out = O / l for the rows that are this unit's tokens
-      bool good = tc::mbar_wait(&S->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1);
-      good = __all_sync(0xffffffffu, good);
+      if (alive) alive = __all_sync(0xffffffffu, tc::mbar_wait(&S->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1));
       tc::tc_fence_after();
       S->red_l[hc][row] = l;
       tc::named_sync(1 + q4, 64);
       const float inv = 1.f / (S->red_l[0][row] + S->red_l[1][row]);
       const bool valid = kPfRows * x.t + row < x.n;
       float* dst = a.out + (static_cast<int64_t>(x.q0 + row) * kH + x.head) * kDh + 64 * hc;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(tm + lane_base + kPaTmO + 64 * hc + c0, r);
+      {
+        uint32_t r0[32], r1[32];
+        tc::tmem_ld32(tm + lane_base + kPaTmO + 64 * hc, r0);
+        tc::tmem_ld32(tm + lane_base + kPaTmO + 64 * hc + 32, r1);
         tc::tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            *reinterpret_cast<float4*>(dst + c0 + c) =
-                make_float4(__uint_as_float(r[c]) * inv, __uint_as_float(r[c + 1]) * inv,
-                            __uint_as_float(r[c + 2]) * inv, __uint_as_float(r[c + 3]) * inv);
+          for (int c = 0; c < 32; c += 4) {
+            *reinterpret_cast<float4*>(dst + c) =
+                make_float4(__uint_as_float(r0[c]) * inv, __uint_as_float(r0[c + 1]) * inv,
+                            __uint_as_float(r0[c + 2]) * inv, __uint_as_float(r0[c + 3]) * inv);
+            *reinterpret_cast<float4*>(dst + 32 + c) =
+                make_float4(__uint_as_float(r1[c]) * inv, __uint_as_float(r1[c + 1]) * inv,
+                            __uint_as_float(r1[c + 2]) * inv, __uint_as_float(r1[c + 3]) * inv);
+          }
         }
       }
-      ok = tc::named_sync_and(5, 32 * kPaSoftmaxWarps, good);
+      ok = tc::named_sync_and(5, 32 * kPaSoftmaxWarps, alive);
     }
     if (!ok) pa_set_abort(S);
   }

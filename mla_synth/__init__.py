@@ -87,9 +87,12 @@ SHAPES = {
     # prefill: 4 prompts of 4096 tokens, each token a query over its prefix
     "prefill_b4": MLAShape("prefill_b4", 4, 128, 512, 64, 128, 64, BF16, BF16, DSV2_W_STD,
                            1.0 / math.sqrt(192), 6, lengths=(4096,) * 4),
+    # one such prompt (the size a profiler capture of the prefill kernels uses)
+    "prefill_b1": MLAShape("prefill_b1", 1, 128, 512, 64, 128, 64, BF16, BF16, DSV2_W_STD,
+                           1.0 / math.sqrt(192), 7, lengths=(4096,)),
 }
 
-PREFILL_SHAPES = ("prefill_b4",)
+PREFILL_SHAPES = ("prefill_b4", "prefill_b1")
 
 
 def shape_with(base: str, **kw) -> MLAShape:
