@@ -363,6 +363,32 @@ def prefill(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_seqs: S
     return out
 
 
+def decode_hidden(q_nope, q_rope, w_uk, w_uv, w_o, c_seqs: Sequence[np.ndarray], kr_seqs: Sequence[np.ndarray],
+                  scale: float, batches: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Attention output projected to the hidden size: u[b] = W_O [o_{b,1}; ...; o_{b,H}] (section
+    2.1.1: the per-head outputs are concatenated and multiplied by the output projection
+    W_O in R^{hidden x (d_h n_h)}), with o_{b,i} the explicit per-head outputs. Returns [B, hidden]
+    (rows of unrequested batches are NaN)."""
+    w_o = np.asarray(w_o, np.float64)
+    q_nope = np.asarray(q_nope, np.float64)
+    B, H, d_h = q_nope.shape
+    per_head = decode(q_nope, q_rope, w_uk, w_uv, c_seqs, kr_seqs, scale, form="explicit", batches=batches)
+    out = np.full((B, w_o.shape[0]), np.nan)
+    for b in (range(B) if batches is None else batches):
+        out[b] = w_o @ per_head[b].reshape(H * d_h)
+    return out
+
+
+def fold_output_weight(w_uv, w_o) -> np.ndarray:
+    """W_UV absorbed into W_O (section 2.1.2): W_OUV[:, i d_c:(i+1) d_c] = W_O[:, i d_h:(i+1) d_h] W_UV_i,
+    so that W_O [W_UV_1 o_1; ...; W_UV_H o_H] = W_OUV [o_1; ...; o_H] for latent-space outputs o_i.
+    Returns [hidden, H d_c]."""
+    w_uv = np.asarray(w_uv, np.float64)
+    w_o = np.asarray(w_o, np.float64)
+    H, d_h, d_c = w_uv.shape
+    return np.concatenate([w_o[:, i * d_h:(i + 1) * d_h] @ w_uv[i] for i in range(H)], axis=1)
+
+
 # ----------------------------------------------------------------------------
 # closed forms from the pages
 

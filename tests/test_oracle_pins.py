@@ -558,3 +558,42 @@ def test_prefill_subset_matches_the_full_result():
                 np.testing.assert_array_equal(part[r, i], full[r, i])
             else:
                 assert np.isnan(part[r, i]).all()
+
+
+def test_hidden_output_is_the_folded_latent_output():
+    # W_O [W_UV_i o_lat_i]_i computed from the explicit outputs equals the fold W_OUV o_lat of the
+    # absorbed form (the output-side absorption of section 2.1.2)
+    rng = np.random.default_rng(15)
+    H, d_h, d_c, d_r, hidden = 3, 4, 6, 2, 7
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    w_o = rng.standard_normal((hidden, H * d_h))
+    lens = [5, 1, 8]
+    cs = [rng.standard_normal((L, d_c)) for L in lens]
+    ks = [rng.standard_normal((L, d_r)) for L in lens]
+    qn, qr = rng.standard_normal((3, H, d_h)), rng.standard_normal((3, H, d_r))
+    got = O.decode_hidden(qn, qr, w_uk, w_uv, w_o, cs, ks, 0.45)
+    w_ouv = O.fold_output_weight(w_uv, w_o)
+    assert w_ouv.shape == (hidden, H * d_c)
+    for b, L in enumerate(lens):
+        o_lat = []
+        for i in range(H):
+            q_lat = w_uk[i].T @ qn[b, i]
+            a = O.softmax_probs(0.45 * (cs[b] @ q_lat + ks[b] @ qr[b, i]))
+            o_lat.append(a @ cs[b])
+        np.testing.assert_allclose(got[b], w_ouv @ np.concatenate(o_lat), rtol=1e-10, atol=1e-12)
+
+
+def test_hidden_output_with_identity_projection_is_the_head_concatenation():
+    rng = np.random.default_rng(16)
+    H, d_h, d_c, d_r = 2, 3, 5, 2
+    w_uk, w_uv = rng.standard_normal((H, d_h, d_c)), rng.standard_normal((H, d_h, d_c))
+    cs, ks = [rng.standard_normal((4, d_c))], [rng.standard_normal((4, d_r))]
+    qn, qr = rng.standard_normal((1, H, d_h)), rng.standard_normal((1, H, d_r))
+    got = O.decode_hidden(qn, qr, w_uk, w_uv, np.eye(H * d_h), cs, ks, 0.6)
+    per_head = O.decode(qn, qr, w_uk, w_uv, cs, ks, 0.6, form="absorbed")
+    np.testing.assert_allclose(got[0], per_head[0].reshape(-1), rtol=1e-11, atol=1e-13)
+    # and a projection that keeps only head 1's first value picks it out
+    w_o = np.zeros((1, H * d_h))
+    w_o[0, d_h] = 1.0
+    np.testing.assert_allclose(O.decode_hidden(qn, qr, w_uk, w_uv, w_o, cs, ks, 0.6)[0, 0], per_head[0, 1, 0],
+                               rtol=1e-12)
