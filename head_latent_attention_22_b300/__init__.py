@@ -21,7 +21,8 @@ import torch
 
 __all__ = ["MLAConfig", "MLAError", "BF16", "FP32", "FP8_E4M3_B128", "library_path", "cache_row_bytes",
            "new_pool", "append", "workspace_size", "workspace_size_multi", "decode", "check_device_errors", "decode_path",
-           "decode_stage_names", "set_stage_events", "decode_static_scratch", "prefill", "prefill_workspace_size"]
+           "decode_stage_names", "set_stage_events", "decode_static_scratch", "prefill", "prefill_workspace_size", "fold_output_weight",
+           "decode_hidden", "decode_hidden_workspace_size"]
 
 BF16, FP32, FP8_E4M3_B128 = 0, 1, 2
 _DTYPE_NAMES = {"bf16": BF16, "fp32": FP32, "fp8_e4m3_b128": FP8_E4M3_B128}
@@ -122,6 +123,9 @@ def _load():
         "mla_decode_multi_workspace_size": (SZ, [CFG, I32, I32, I32, I32]),
         "mla_decode_multi": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, I32, P, P, SZ, P]),
         "mla_prefill_workspace_size": (SZ, [CFG, I32, I32]),
+        "mla_fold_output_weight": (I32, [CFG, P, P, I32, P, P]),
+        "mla_decode_hidden_workspace_size": (SZ, [CFG, I32, I32, I32]),
+        "mla_decode_hidden": (I32, [CFG, P, P, P, P, P, I64, P, P, I32, I32, I32, I32, P, P, SZ, P]),
         "mla_prefill": (I32, [CFG, P, P, P, P, P, I64, P, P, P, I32, I32, I32, I32, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
@@ -354,6 +358,65 @@ def prefill(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: to
                                _ptr(pool), pool.shape[0], _ptr(block_table), _ptr(seq_lens), _ptr(q_start), B,
                                max_pages, max_seq_len, T, _ptr(out), _ptr(workspace), workspace.numel(),
                                _stream(stream)))
+    return out
+
+
+def fold_output_weight(cfg: MLAConfig, w_uv: torch.Tensor, w_o: torch.Tensor,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """mla_fold_output_weight: W_OUV [hidden, H * d_c] fp16 with W_OUV[:, i d_c:(i+1) d_c] = W_O[:, i d_h:(i+1) d_h] W_UV[i].
+
+    w_o [hidden, H * d_head] (the output projection), w_uv [H, d_head, d_c]."""
+    dt = cfg.io_torch_dtype
+    _need(w_uv, "w_uv", dt, 3)
+    _need(w_o, "w_o", dt, 2)
+    hidden = w_o.shape[0]
+    if w_o.shape[1] != cfg.n_heads * cfg.d_head:
+        raise ValueError("w_o must be [hidden, n_heads * d_head]")
+    if out is None:
+        out = torch.empty((hidden, cfg.n_heads * cfg.d_c), dtype=torch.float16, device=w_o.device)
+    _need(out, "out", torch.float16, 2)
+    _check(_load().mla_fold_output_weight(ctypes.byref(cfg.c()), _ptr(w_uv), _ptr(w_o), hidden, _ptr(out),
+                                          _stream(stream)))
+    return out
+
+
+def decode_hidden_workspace_size(cfg: MLAConfig, batch: int, max_seq_len: int, hidden: int) -> int:
+    return int(_load().mla_decode_hidden_workspace_size(ctypes.byref(cfg.c()), batch, max_seq_len, hidden))
+
+
+def decode_hidden(cfg: MLAConfig, q_nope: torch.Tensor, q_rope: torch.Tensor, w_uk: torch.Tensor,
+                  w_ouv: torch.Tensor, pool: torch.Tensor, block_table: Optional[torch.Tensor], seq_lens: torch.Tensor,
+                  max_seq_len: int, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  max_pages: Optional[int] = None, stream=None) -> torch.Tensor:
+    """mla_decode_hidden: the decode with W_UV folded into W_O -> [B, hidden] fp32 (w_ouv from
+    fold_output_weight)."""
+    dt = cfg.io_torch_dtype
+    _need(q_nope, "q_nope", dt, 3)
+    _need(q_rope, "q_rope", dt, 3)
+    _need(w_uk, "w_uk", dt, 3)
+    _need(w_ouv, "w_ouv", torch.float16, 2)
+    _need(pool, "pool", torch.uint8)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B = q_nope.shape[0]
+    hidden = w_ouv.shape[0]
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        max_pages = block_table.shape[1]
+    if max_pages is None:
+        raise ValueError("max_pages is needed without a block table")
+    if out is None:
+        out = torch.empty((B, hidden), dtype=torch.float32, device=q_nope.device)
+    _need(out, "out", torch.float32, 2)
+    need = decode_hidden_workspace_size(cfg, B, max_seq_len, hidden)
+    if need == 0:
+        raise MLAError(2, "no folded output path for this config or size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_nope.device)
+    _need(workspace, "workspace", torch.uint8)
+    _check(_load().mla_decode_hidden(ctypes.byref(cfg.c()), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(w_ouv),
+                                     _ptr(pool), pool.shape[0], _ptr(block_table), _ptr(seq_lens), B, max_pages,
+                                     max_seq_len, hidden, _ptr(out), _ptr(workspace), workspace.numel(),
+                                     _stream(stream)))
     return out
 
 

@@ -298,9 +298,10 @@ struct MergeArgs {
   Plan plan;
   const float* part_o;   // chunk-major, see parto_index
   const float* part_ml;  // [slots, H, 2]
-  uint16_t* o_hi;        // [B, H, 512] bf16: o_lat rounded
-  uint16_t* o_lo;        // [B, H, 512] bf16: o_lat - o_hi rounded
+  uint16_t* o_hi;        // [B, H, 512] bf16 (fp16 when f16): o_lat rounded
+  uint16_t* o_lo;        // [B, H, 512] bf16 (fp16 when f16): o_lat - o_hi rounded
   int batch, ncl;
+  int f16;               // 1: fp16 pair (the operand type of the folded output GEMM)
 };
 
 constexpr int kMergeSplit = kOChunks;            // CTAs per sequence: one 4-float chunk each
@@ -358,11 +359,22 @@ __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
   const float inv = den > 0.f ? 1.f / den : 0.f;
   const float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
   uint32_t hi[2], lo[2];
+  if (a.f16) {
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
-    lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
-                          v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
+    for (int u = 0; u < 2; ++u) {
+      const __half h0 = __float2half_rn(v[2 * u]), h1 = __float2half_rn(v[2 * u + 1]);
+      const __half l0 = __float2half_rn(v[2 * u] - __half2float(h0));
+      const __half l1 = __float2half_rn(v[2 * u + 1] - __half2float(h1));
+      hi[u] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+      lo[u] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
+      lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
+                            v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
+    }
   }
   const int64_t e = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * chunk;
   *reinterpret_cast<uint2*>(a.o_hi + e) = make_uint2(hi[0], hi[1]);

@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "decode_simt.cuh"
 #include "decode_tc.cuh"
+#include "fold.cuh"
 #include "prefill.cuh"
 #include "tmap.cuh"
 
@@ -339,13 +340,27 @@ mla_status launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaSt
   return MLA_OK;
 }
 
+// Split of the hidden-output GEMM's 65,536-wide contraction: about two waves of two CTAs per SM.
+int out_groups(int hidden) {
+  const int m_tiles = hidden / 128;
+  const int want = (4 * current_sm_count() + m_tiles - 1) / m_tiles;
+  return want < 1 ? 1 : (want > 64 ? 64 : want);
+}
+
+size_t out_partial_bytes(int batch, int hidden) {
+  return align_up(static_cast<size_t>(out_groups(hidden)) * batch * hidden * 4, 256);
+}
+
+// w_ouv == NULL: the per-head outputs out[B, H, d_h] (W_UV after the merge). Otherwise W_UV folded into
+// W_O: out[B, hidden] = W_OUV o_lat.
 mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope, const void* w_uk, const void* w_uv,
                      const void* pool, int64_t num_pages, const int32_t* block_table, const int32_t* seq_lens,
                      int batch, int max_pages, int max_seq_len, float* out, void* workspace, size_t workspace_bytes,
-                     cudaStream_t st) {
+                     cudaStream_t st, const void* w_ouv = nullptr, int hidden = 0) {
   const TcPlan p = tc_plan(batch);
-  if (workspace_bytes < p.bytes)
-    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, p.bytes);
+  const size_t need = p.bytes + (w_ouv ? out_partial_bytes(batch, hidden) : 0);
+  if (workspace_bytes < need)
+    return fail(MLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
   const int64_t pool_rows = num_pages * static_cast<int64_t>(c->page_size);
   if (pool_rows >= (static_cast<int64_t>(1) << 31))
     return fail(MLA_ERR_UNSUPPORTED, "pool of %lld rows exceeds the 2^31 rows a tile coordinate can address",
@@ -391,9 +406,21 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                         SW) &&
             make_map_2d(&m_qr, q_lat, BF, tcd::kRow, static_cast<uint64_t>(batch) * tcd::kH, tcd::kRow * 2, 32, 16,
                         SW64);
+  const int out_nb = (batch + 15) / 16 * 16;
+  const CUtensorMapDataType F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap m_wouv, m_ohi, m_olo;
+  if (w_ouv)
+    maps_ok = maps_ok &&
+              make_map_2d(&m_wouv, w_ouv, F16, static_cast<uint64_t>(tcd::kH) * tcd::kDc, static_cast<uint64_t>(hidden),
+                          static_cast<uint64_t>(tcd::kH) * tcd::kDc * 2, 64, 128, SW) &&
+              make_map_2d(&m_ohi, o_hi, F16, tcd::kH * tcd::kDc, static_cast<uint64_t>(batch), tcd::kH * tcd::kDc * 2, 64,
+                          static_cast<uint32_t>(out_nb), SW) &&
+              make_map_2d(&m_olo, o_lo, F16, tcd::kH * tcd::kDc, static_cast<uint64_t>(batch), tcd::kH * tcd::kDc * 2, 64,
+                          static_cast<uint32_t>(out_nb), SW);
+  else
+    maps_ok = maps_ok && make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW);
   if (!maps_ok ||
       !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
-      !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, tcd::kH * tcd::kDh, tcd::kDc * 2, 64, tcd::kDh, SW) ||
       !make_map_2d(&m_qn, q_nope, BF, tcd::kH * tcd::kDh, static_cast<uint64_t>(batch), tcd::kH * tcd::kDh * 2, 64,
                    static_cast<uint32_t>(p.nb), SW) ||
       !make_map_2d(&m_hi, o_hi, BF, tcd::kH * tcd::kDc, static_cast<uint64_t>(batch), tcd::kH * tcd::kDc * 2, 64,
@@ -434,6 +461,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   ma.o_lo = o_lo;
   ma.batch = batch;
   ma.ncl = ncl;
+  ma.f16 = w_ouv ? 1 : 0;
 
   tcd::UvArgs ua{};
   ua.out = out;
@@ -459,6 +487,33 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
                  st, merge_args);
   if (s != MLA_OK) return s;
   stage_mark(3, st);
+  if (w_ouv) {
+    tcd::OutArgs oa{};
+    oa.partial = reinterpret_cast<float*>(ws + p.bytes);
+    oa.batch = batch;
+    oa.nb = out_nb;
+    oa.hidden = hidden;
+    oa.n_groups = out_groups(hidden);
+    const size_t osm = tcd::out_smem_bytes(out_nb);
+    cudaError_t e = cudaFuncSetAttribute(tcd::out_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(osm));
+    if (e != cudaSuccess) return cuda_fail(e, "out_tc smem attribute");
+    void* out_args[] = {&m_wouv, &m_ohi, &m_olo, &oa};
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::out_tc_kernel), dim3(hidden / 128, oa.n_groups),
+                   dim3(tcd::kOutThreads), osm, st, out_args);
+    if (s != MLA_OK) return s;
+    stage_mark(4, st);
+    const float* part = oa.partial;
+    int groups = oa.n_groups;
+    int64_t count = static_cast<int64_t>(batch) * hidden;
+    void* red_args[] = {&part, &out, &groups, &count};
+    const int64_t want = (count + 255) / 256;
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::out_reduce_kernel), dim3(static_cast<unsigned>(want < 1184 ? want : 1184)),
+                   dim3(256), 0, st, red_args);
+    if (s != MLA_OK) return s;
+    stage_mark(5, st);
+    return MLA_OK;
+  }
   void* uv_args[] = {&m_wuv, &m_hi, &m_lo, &ua};
   s = launch_pdl(reinterpret_cast<const void*>(tcd::uv_tc_kernel), dim3(tcd::kH), dim3(tcd::kUvThreads), kUvSmem, st,
                  uv_args);
@@ -771,6 +826,53 @@ mla_status mla_decode_static_scratch(const mla_config* cfg, const void* q_nope, 
   if (s != MLA_OK) return s;
   return mla_decode(cfg, q_nope, q_rope, w_uk, w_uv, pool, num_pages, block_table, seq_lens, batch, max_pages,
                     max_seq_len, out, scratch, MLA_STATIC_SCRATCH_BYTES, stream);
+}
+
+mla_status mla_fold_output_weight(const mla_config* cfg, const void* w_uv, const void* w_o, int32_t hidden,
+                                  void* w_ouv, void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (!tc_supported(cfg))
+    return fail(MLA_ERR_UNSUPPORTED, "the folded output projection runs the DeepSeek-V2 shape with bf16 weights");
+  if (hidden < 128 || hidden % 128 != 0) return fail(MLA_ERR_INVALID_ARG, "hidden must be a positive multiple of 128");
+  if (!w_uv || !w_o || !w_ouv) return fail(MLA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(w_uv) || !aligned16(w_o) || !aligned16(w_ouv))
+    return fail(MLA_ERR_INVALID_ARG, "w_uv, w_o and w_ouv must be 16-byte aligned");
+  tcd::fold_wo_kernel<<<dim3(hidden / tcd::kFoldTile, tcd::kDc / tcd::kFoldTile, tcd::kH), 256, 0, as_stream(stream)>>>(
+      static_cast<const uint16_t*>(w_uv), static_cast<const uint16_t*>(w_o), static_cast<uint16_t*>(w_ouv), hidden);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fold launch");
+  return MLA_OK;
+}
+
+size_t mla_decode_hidden_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len, int32_t hidden) {
+  if (check_config(cfg) != MLA_OK || !tc_supported(cfg) || batch < 1 || batch > tcd::kOutMaxNb || max_seq_len < 0 ||
+      hidden < 128 || hidden % 128 != 0)
+    return 0;
+  return tc_plan(batch).bytes + out_partial_bytes(batch, hidden);
+}
+
+mla_status mla_decode_hidden(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
+                             const void* w_ouv, const void* pool, int64_t num_pages, const int32_t* block_table,
+                             const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t max_seq_len,
+                             int32_t hidden, float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  mla_status s = check_config(cfg);
+  if (s != MLA_OK) return s;
+  if (!tc_supported(cfg))
+    return fail(MLA_ERR_UNSUPPORTED, "the folded output projection runs the DeepSeek-V2 shape with bf16 weights");
+  if (batch < 1 || batch > tcd::kOutMaxNb || max_pages < 1 || num_pages < 1 || max_seq_len < 0 || hidden < 128 ||
+      hidden % 128 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: batch=%d (1..%d) max_pages=%d num_pages=%lld max_seq_len=%d hidden=%d",
+                batch, tcd::kOutMaxNb, max_pages, static_cast<long long>(num_pages), max_seq_len, hidden);
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * cfg->page_size)
+    return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d exceeds max_pages * page_size", max_seq_len);
+  if (!q_nope || !q_rope || !w_uk || !w_ouv || !pool || !seq_lens || !out || !workspace)
+    return fail(MLA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(w_ouv) || !aligned16(pool) ||
+      !aligned16(out) || !aligned16(workspace))
+    return fail(MLA_ERR_INVALID_ARG, "q_nope, q_rope, w_uk, w_ouv, pool, out and workspace must be 16-byte aligned");
+  return decode_tc(cfg, q_nope, q_rope, w_uk, nullptr, pool, num_pages, block_table, seq_lens, batch, max_pages,
+                   max_seq_len, out, workspace, workspace_bytes, as_stream(stream), w_ouv, hidden);
 }
 
 size_t mla_prefill_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len) {

@@ -238,6 +238,36 @@ MLA_API mla_status mla_decode_static_scratch(const mla_config* cfg, const void* 
                                              int32_t max_seq_len, float* out, void* stream);
 
 /*
+ * W_UV folded into the output projection W_O (DeepSeek-V2 report, section
+ * 2.1.2: W_UV can be absorbed into W_O; section 2.1.1: u = W_O [o_1; ...; o_H]).
+ *
+ * mla_fold_output_weight - once per set of weights:
+ *   w_ouv[:, i d_c .. (i+1) d_c) = w_o[:, i d_h .. (i+1) d_h) w_uv[i]   (fp32 sums, rounded to io_dtype)
+ *   w_uv  [n_heads, d_head, d_c], w_o [hidden, n_heads * d_head] (row-major) in io_dtype;
+ *   w_ouv [hidden, n_heads * d_c] written in fp16 (IEEE binary16, round to nearest even): the folded
+ *   products are of the order |W_O| |W_UV| sqrt(d_head), where fp16 keeps 3 more bits than bf16.
+ *   hidden a positive multiple of 128 (5120 for DeepSeek-V2). Runs on CUDA cores (not a decode step).
+ *
+ * mla_decode_hidden - mla_decode with the output taken to the hidden size:
+ *   out[b, :] = w_ouv [o_lat(b, 1); ...; o_lat(b, H)]  (= W_O [o(b, 1); ...; o(b, H)]), fp32 [batch, hidden]
+ * where o_lat(b, i) is head i's attention-weighted latent; one GEMM over the 65,536-wide latent outputs
+ * replaces the W_UV step and the caller's W_O GEMM. Arguments as mla_decode, with w_ouv in place of w_uv;
+ * the workspace is mla_decode_hidden_workspace_size() bytes (0 for an unsupported config or size).
+ * Supported: the tensor-core decode path's configs, batch 1 .. 128. As with W_UK, the GEMM may start
+ * reading w_ouv before the kernel that precedes the call on `stream` has finished, so that kernel must
+ * not write it.
+ */
+MLA_API mla_status mla_fold_output_weight(const mla_config* cfg, const void* w_uv, const void* w_o, int32_t hidden,
+                                          void* w_ouv, void* stream);
+MLA_API size_t mla_decode_hidden_workspace_size(const mla_config* cfg, int32_t batch, int32_t max_seq_len,
+                                                int32_t hidden);
+MLA_API mla_status mla_decode_hidden(const mla_config* cfg, const void* q_nope, const void* q_rope, const void* w_uk,
+                                     const void* w_ouv, const void* pool, int64_t num_pages,
+                                     const int32_t* block_table, const int32_t* seq_lens, int32_t batch,
+                                     int32_t max_pages, int32_t max_seq_len, int32_t hidden, float* out,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mla_prefill - attention of whole prompts (or prompt chunks) over the
  * paged latent cache, in the non-absorbed form of the DeepSeek-V2 report,
  * section 2.1.2 (per-head keys k_{j,i} = W_UK,i c_j and values

@@ -280,3 +280,10 @@ def draw_prefill(inp: MLAInputs, n_new: Optional[np.ndarray] = None, step: int =
     dt = torch_dtype(s.io_dtype)
     return PrefillInputs(_normal(gen, (T, s.n_heads, s.d_head), 1.0, dt),
                          _normal(gen, (T, s.n_heads, s.d_rope), 1.0, dt), n, qs)
+
+
+def draw_w_o(shape: MLAShape, hidden: int = 5120, seed: int = 0) -> torch.Tensor:
+    """Output projection W_O [hidden, n_heads * d_head] in io dtype, N(0, 0.006^2) (the report's
+    initialisation std, section 3.1.2)."""
+    gen = torch.Generator().manual_seed(4_000_037 + 101 * seed + shape.seed)
+    return _normal(gen, (hidden, shape.n_heads * shape.d_head), 0.006, torch_dtype(shape.io_dtype))

@@ -364,15 +364,15 @@ def prefill(q_nope, q_rope, w_uk, w_uv, c_seqs: Sequence[np.ndarray], kr_seqs: S
 
 
 def decode_hidden(q_nope, q_rope, w_uk, w_uv, w_o, c_seqs: Sequence[np.ndarray], kr_seqs: Sequence[np.ndarray],
-                  scale: float, batches: Optional[Sequence[int]] = None) -> np.ndarray:
+                  scale: float, batches: Optional[Sequence[int]] = None, form: str = "explicit") -> np.ndarray:
     """Attention output projected to the hidden size: u[b] = W_O [o_{b,1}; ...; o_{b,H}] (section
     2.1.1: the per-head outputs are concatenated and multiplied by the output projection
-    W_O in R^{hidden x (d_h n_h)}), with o_{b,i} the explicit per-head outputs. Returns [B, hidden]
-    (rows of unrequested batches are NaN)."""
+    W_O in R^{hidden x (d_h n_h)}), with o_{b,i} the per-head outputs (explicit form by default; the
+    absorbed form gives the same values). Returns [B, hidden] (rows of unrequested batches are NaN)."""
     w_o = np.asarray(w_o, np.float64)
     q_nope = np.asarray(q_nope, np.float64)
     B, H, d_h = q_nope.shape
-    per_head = decode(q_nope, q_rope, w_uk, w_uv, c_seqs, kr_seqs, scale, form="explicit", batches=batches)
+    per_head = decode(q_nope, q_rope, w_uk, w_uv, c_seqs, kr_seqs, scale, form=form, batches=batches)
     out = np.full((B, w_o.shape[0]), np.nan)
     for b in (range(B) if batches is None else batches):
         out[b] = w_o @ per_head[b].reshape(H * d_h)
