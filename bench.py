@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens decoded per sequence per step (multi-token prediction drafts); 1 = plain decode")
+    ap.add_argument("--hidden", type=int, default=0,
+                    help="take the decode output to this hidden size with W_UV folded into W_O (mla_decode_hidden)")
     return ap.parse_args()
 
 
@@ -176,6 +178,14 @@ def committed_traffic(kernel: str, workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def out_groups_guess(hidden: int) -> int:
+    """Contraction slices of the folded output GEMM (as the library picks them for this GPU); each
+    writes one fp32 partial of [batch, hidden]."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    m_tiles = hidden // 128
+    return max(1, min(64, (4 * sms + m_tiles - 1) // m_tiles))
+
+
 def peaks():
     try:
         p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -219,7 +229,15 @@ def run_gpu(args, rank, world, local):
     # the step's new tokens are each sequence's last q rows (rewritten by the step's append)
     new_pos = torch.from_numpy(np.array([int(L) - q + k for L in inp.lengths for k in range(q)], np.int32)).to(dev)
     new_seq = torch.from_numpy(np.repeat(np.arange(B_, dtype=np.int32), q)).to(dev)
-    if q == 1:
+    hid = args.hidden
+    if hid:
+        if q != 1:
+            raise SystemExit("--hidden runs the single-token decode")
+        w_ouv = M.fold_output_weight(cfg, w_uv, S.draw_w_o(shape, hid).to(dev))
+        out = torch.empty((B_, hid), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, M.decode_hidden_workspace_size(cfg, B_, max_len, hid)), dtype=torch.uint8,
+                         device=dev)
+    elif q == 1:
         out = torch.empty((B_, H, shape.d_head), dtype=torch.float32, device=dev)
         ws = torch.empty(max(256, M.workspace_size(cfg, B_, max_len)), dtype=torch.uint8, device=dev)
     else:
@@ -240,12 +258,17 @@ def run_gpu(args, rank, world, local):
     def step(k, tensors=None):
         qn, qr, cn, kn = dsteps[k % len(dsteps)] if tensors is None else tensors
         M.append(cfg, cn, kn, new_pos, pool, bt, seq_idx=new_seq)
-        if q == 1:
+        if hid:
+            M.decode_hidden(cfg, qn, qr, w_uk, w_ouv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        elif q == 1:
             M.decode(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
         else:
             M.decode_multi(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
 
-    launches_per_step = 1 + (q > 1) + len(M.decode_stage_names(cfg))
+    names = M.decode_stage_names(cfg)
+    if hid:
+        names = names[:3] + ["out_tc", "out_reduce"]
+    launches_per_step = 1 + (q > 1) + len(names)
     for k in range(args.warmup):
         step(k)
         flush_l2()
@@ -274,7 +297,6 @@ def run_gpu(args, rank, world, local):
     # per-kernel durations (separate pass, same steps, events between the kernels). A GPU-side
     # sleep ahead of each step lets the host enqueue all of the step's launches and events before
     # the first event fires, so an interval holds its kernel's GPU time and no host enqueue gap.
-    names = M.decode_stage_names(cfg)
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush_l2()
@@ -295,6 +317,9 @@ def run_gpu(args, rank, world, local):
     weight_bytes = 2 * H * shape.d_head * shape.d_c * (2 if shape.io_dtype == "bf16" else 4)
     if dom.startswith("attend"):
         alg_bytes, alg_flop = attend_bytes, attend_flop
+    elif dom == "out_tc":
+        alg_bytes = hid * H * shape.d_c * 2 + 2 * B_ * H * shape.d_c * 2 + 4 * B_ * hid * out_groups_guess(hid)
+        alg_flop = 2 * 2 * B_ * hid * H * shape.d_c
     else:
         alg_bytes, alg_flop = weight_bytes / 2, 2 * B_ * H * shape.d_head * shape.d_c
     t = per_kernel[dom] / 1e3
@@ -315,6 +340,9 @@ def run_gpu(args, rank, world, local):
     # whole-step roofline: the slower of all bytes over HBM and all FLOPs over the tensor peak
     step_bytes = attend_bytes + weight_bytes + B_ * q * row
     step_flop = attend_flop + 4 * B_ * q * H * shape.d_head * shape.d_c
+    if hid:   # W_UV's bytes and FLOPs replaced by the folded weight's (hi and lo operands of o_lat)
+        step_bytes += hid * H * shape.d_c * 2 - weight_bytes / 2
+        step_flop += 2 * 2 * B_ * hid * H * shape.d_c - 2 * B_ * H * shape.d_head * shape.d_c
     t_roof = max(step_bytes / (hbm * 1e9), step_flop / (tf_burst * 1e12))
     roofline["step_frac"] = round(t_roof / (ms_per_step / 1e3), 4)
 
@@ -338,7 +366,7 @@ def run_gpu(args, rank, world, local):
     dv = [dblk[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(srcs[0], offs, nbytes)]
     dv_q_nope, dv_q_rope, dv_c_new, dv_k_new = dv
     dblk.copy_(host[0])
-    if q == 1:
+    if q == 1 and not hid:
         graph = M.StepGraph(cfg, c_new=dv_c_new, k_new=dv_k_new, positions=new_pos, seq_idx=new_seq,
                             q_nope=dv_q_nope, q_rope=dv_q_rope, w_uk=w_uk, w_uv=w_uv, pool=pool, block_table=bt,
                             seq_lens=seq_lens, max_seq_len=max_len, out=out, workspace=ws)
@@ -376,6 +404,7 @@ def run_gpu(args, rank, world, local):
                       "attended_tokens_per_step": tokens,
                       "n_heads": H, "d_c": shape.d_c, "d_rope": shape.d_rope, "d_head": shape.d_head,
                       "page_size": shape.page_size, "cache_dtype": shape.cache_dtype, "q_len": q,
+                      "output": f"hidden {hid} (W_UV folded into W_O)" if hid else "per-head [B, H, d_head]",
                       "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB memset + 512 MiB read)",
                       "decode_path": "tcgen05" if M.decode_path(cfg) else "cuda-core"},
            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,

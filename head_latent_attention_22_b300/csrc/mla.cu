@@ -588,10 +588,10 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
       !make_map_2d(&m_qn, q_nope, BF, wkv, static_cast<uint64_t>(n_tokens), wkv * 2, 64, tcd::kPfRows, SW) ||
       !make_map_2d(&m_qr, q_rope, BF, static_cast<uint64_t>(tcd::kH) * tcd::kDr, static_cast<uint64_t>(n_tokens),
                    static_cast<uint64_t>(tcd::kH) * tcd::kDr * 2, 64, tcd::kPfRows, SW) ||
-      !make_map_2d(&m_k, k_buf, BF, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64, tcd::kPfRows, SW) ||
+      !make_map_2d(&m_k, k_buf, BF, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64, 64, SW) ||
       !make_map_2d(&m_v, v_buf, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wkv, static_cast<uint64_t>(kv_rows), wkv * 2, 64,
                    tcd::kPfRows, SW) ||
-      !make_map_2d(&m_kr, kr_buf, BF, tcd::kDr, static_cast<uint64_t>(kv_rows), tcd::kDr * 2, 64, tcd::kPfRows, SW))
+      !make_map_2d(&m_kr, kr_buf, BF, tcd::kDr, static_cast<uint64_t>(kv_rows), tcd::kDr * 2, 64, 64, SW))
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled refused a tensor description (or the driver entry point is missing)");
 
   tcd::KvUpArgs ka{};
@@ -620,14 +620,18 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
   pa.max_seq_len = max_seq_len;
   pa.lpad = p.lpad;
   pa.n_tokens = n_tokens;
-  pa.qt_max = p.lpad / tcd::kPfRows;
+  pa.qp_max = (p.lpad + 2 * tcd::kPfRows - 1) / (2 * tcd::kPfRows);
   pa.scale_log2 = softmax_scale(c) * 1.4426950408889634f;
 
   const int sms = current_sm_count();
   const int64_t items = static_cast<int64_t>(p.lpad / tcd::kPfRows) * batch * tcd::kKvGroups;
   const int g_kv = static_cast<int>(items < sms ? items : sms);
-  const int64_t units = static_cast<int64_t>(batch) * tcd::kH * pa.qt_max;
-  const int g_pa = static_cast<int>(units < sms ? units : sms);
+  const int64_t units = static_cast<int64_t>(batch) * tcd::kH * pa.qp_max;
+  int pa_clusters = 0;
+  mla_status cs = cluster_count(reinterpret_cast<const void*>(tcd::prefill_attn_kernel), tcd::kPaThreads, tcd::kPaSmem,
+                                &pa_clusters);
+  if (cs != MLA_OK) return cs;
+  if (units < pa_clusters) pa_clusters = static_cast<int>(units);
   stage_mark(0, st);
   void* kv_args[] = {&m_lat, &m_wuk, &m_wuv, &ka};
   mla_status s = launch_pdl(reinterpret_cast<const void*>(tcd::kv_up_kernel), dim3(g_kv), dim3(tcd::kKvThreads),
@@ -635,8 +639,8 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
   if (s != MLA_OK) return s;
   stage_mark(1, st);
   void* pa_args[] = {&m_qn, &m_qr, &m_k, &m_v, &m_kr, &pa};
-  s = launch_pdl(reinterpret_cast<const void*>(tcd::prefill_attn_kernel), dim3(g_pa), dim3(tcd::kPaThreads),
-                 tcd::kPaSmem, st, pa_args);
+  s = launch_pdl(reinterpret_cast<const void*>(tcd::prefill_attn_kernel), dim3(2 * pa_clusters),
+                 dim3(tcd::kPaThreads), tcd::kPaSmem, st, pa_args);
   if (s != MLA_OK) return s;
   stage_mark(2, st);
   return MLA_OK;

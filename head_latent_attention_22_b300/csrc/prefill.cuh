@@ -20,10 +20,11 @@
 //                        M = 128 rows, N = 256, K = 16; fp32 accumulators in
 //                        TMEM, two of them so the epilogue of one column
 //                        tile overlaps the MMAs of the next.
-//   prefill_attn_kernel: per (sequence, head, 128-row query tile): S = Q K^T
-//                        (M = N = 128, K = 192, bf16), online softmax with a
-//                        causal mask, O += P V (M = N = 128, K = 128, fp16,
-//                        P from TMEM), out = O / l in fp32.
+//   prefill_attn_kernel: per (sequence, head, 256 query rows) on a CTA pair:
+//                        S = Q K^T (pair MMA, M = 256, N = 128 keys,
+//                        K = 192, bf16), online softmax with a causal mask,
+//                        O += P V (pair MMA, M = 256, N = 128, K = 128 keys,
+//                        fp16, P from TMEM), out = O / l in fp32.
 //
 // V and P are fp16 rather than bf16: with few keys (the first tokens of a
 // prompt) a weighted sum does not average the rounding of its terms away,
@@ -320,28 +321,48 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 }
 
 // ------------------------------------------------------------------ prefill_attn_kernel
-constexpr int kPaStages = 2;                          // ring depth of key tiles and of value tiles
-constexpr int kPaQBytes = 3 * kPfBox;                 // q_nope (2 boxes) and q_rope (1 box) of 128 rows: 48 KB
-constexpr int kPaKBytes = 3 * kPfBox;                 // k_nope (2 boxes) and the shared rope key (1 box)
-constexpr int kPaVBytes = 2 * kPfBox;                 // V: 2 boxes of 128 rows x 64 columns
+// A cluster of two CTAs works on 256 query rows of one (sequence, head): CTA r holds rows
+// 128 r .. 128 r + 127 and issues nothing; the even CTA issues pair MMAs (tcgen05 cta_group::2) for
+// both. In the score MMA each CTA supplies half of the key tile's rows (64 keys) and in the PV MMA
+// half of the value columns (64 of d_h), so a CTA loads 40 KB per 128-key tile where one CTA
+// working alone loads 80 KB: a tile load is then shorter than the tile's MMAs (one SM's tensor
+// memory access pipe moves about 34 bytes per cycle).
+constexpr int kPaKStages = 4;                         // ring depth of key tiles
+constexpr int kPaVStages = 4;                         // ring depth of value tiles
+constexpr int kPaQBytes = 3 * kPfBox;                 // this CTA's 128 query rows: q_nope (2 boxes), q_rope
+constexpr int kPaKBytes = 3 * kPfHalfBox;             // this CTA's 64 keys: k_nope (2 boxes), rope key (1 box)
+constexpr int kPaVBytes = kPfBox;                     // all 128 keys x this CTA's 64 value columns
 constexpr int kPaSoftmaxWarps = 8;
-constexpr int kPaThreads = 32 * (kPaSoftmaxWarps + 2);
+constexpr int kPaL2Ahead = 4;                         // tiles a key/value tile is prefetched to L2 ahead of its load
+constexpr int kPaThreads = 32 * (kPaSoftmaxWarps + 4);   // softmax 0-7, producer 8, S MMAs 9, forwarder 10, PV MMAs 11
 constexpr uint32_t kPaTmS = 0;     // score buffers: columns 0 and 128
-constexpr uint32_t kPaTmP = 256;   // P buffers (bf16 pairs): columns 256 and 320
+constexpr uint32_t kPaTmP = 256;   // P buffers (fp16 pairs): columns 256 and 320
 constexpr uint32_t kPaTmO = 384;   // O: 128 columns
 
 struct PaSmem {
-  uint64_t q_full, q_empty;
-  uint64_t k_full[kPaStages], k_empty[kPaStages], v_full[kPaStages], v_empty[kPaStages];
+  uint64_t q_full, q_empty, q_ready;
+  uint64_t k_full[kPaKStages], k_empty[kPaKStages], k_ready[kPaKStages];
+  uint64_t v_full[kPaVStages], v_empty[kPaVStages], v_ready[kPaVStages];
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2];
-  uint64_t drain;
+  uint64_t drain[2];
   float red_max[2][2][kPfRows];   // [tile parity][column half][row]
   float red_l[2][kPfRows];        // [column half][row]
   uint32_t tmem_base;
   int32_t abort_flag;
 };
-constexpr size_t kPaSmem =
-    1024 + kPaQBytes + static_cast<size_t>(kPaStages) * (kPaKBytes + kPaVBytes) + sizeof(PaSmem);
+constexpr size_t kPaSmem = 1024 + kPaQBytes + static_cast<size_t>(kPaKStages) * kPaKBytes +
+                           static_cast<size_t>(kPaVStages) * kPaVBytes + sizeof(PaSmem);
+
+// Pair MMA with A (P) in tensor memory: each CTA's rows at the same TMEM address.
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 struct PrefillArgs {
   const int32_t* block_table;
@@ -349,34 +370,34 @@ struct PrefillArgs {
   const int32_t* q_start;    // [B + 1] new tokens of sequence b are rows q_start[b] .. q_start[b+1]-1
   float* out;                // [T, 128, 128] fp32
   int64_t num_pages;
-  int batch, max_pages, page_size, max_seq_len, lpad, n_tokens, qt_max;
+  int batch, max_pages, page_size, max_seq_len, lpad, n_tokens, qp_max;
   float scale_log2;
 };
 
-// Unit u: query tile t of (sequence b, head). Units of one (sequence, head) are consecutive
-// (longest tile first), so the CTAs working at one time share a few heads' K and V in L2.
+// Unit u: query rows 256 t .. 256 t + 255 of (sequence b, head). Units of one (sequence, head) are
+// consecutive (longest first), so the clusters working at one time share a few heads' K and V in L2.
 struct PaUnit {
-  int b, t, head, nk, n, p0, q0;
+  int b, t, head, nk, n, p0, q0;   // q0: first query row of the pair (this CTA adds 128 rank)
   bool live;
 };
 __device__ __forceinline__ PaUnit pa_unit(const PrefillArgs& a, int64_t u) {
   PaUnit x;
-  const int64_t grp = u / a.qt_max;
-  x.t = a.qt_max - 1 - static_cast<int>(u % a.qt_max);
+  const int64_t grp = u / a.qp_max;
+  x.t = a.qp_max - 1 - static_cast<int>(u % a.qp_max);
   x.b = static_cast<int>(grp / kH);
   x.head = static_cast<int>(grp % kH);
   const int L = clamp_len(a.seq_lens[x.b], a.max_seq_len);
   const int s0 = a.q_start[x.b], s1 = a.q_start[x.b + 1];
   x.n = s1 - s0;
-  x.q0 = s0 + kPfRows * x.t;
+  x.q0 = s0 + 2 * kPfRows * x.t;
   x.p0 = L - x.n;
-  x.live = x.n > 0 && x.n <= L && s0 >= 0 && s1 <= a.n_tokens && kPfRows * x.t < x.n;
+  x.live = x.n > 0 && x.n <= L && s0 >= 0 && s1 <= a.n_tokens && 2 * kPfRows * x.t < x.n;
   if (!x.live) {
     if (x.t == 0 && x.head == 0 && (x.n < 0 || x.n > L || s0 < 0 || s1 > a.n_tokens)) flag_error(ERR_BIT_BOUNDS);
     x.nk = 0;
     return x;
   }
-  const int last = x.p0 + min(x.n, kPfRows * (x.t + 1)) - 1;   // position of the tile's last query row
+  const int last = x.p0 + min(x.n, 2 * kPfRows * (x.t + 1)) - 1;   // position of the pair's last query row
   x.nk = last / kPfRows + 1;
   return x;
 }
@@ -386,36 +407,44 @@ __device__ __forceinline__ bool pa_aborted(const PaSmem* s) {
 }
 __device__ __forceinline__ void pa_set_abort(PaSmem* s) { *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1; }
 
-// map_qn: q_nope [T, 128 * 128] bf16; map_qr: q_rope [T, 128 * 64]; map_k / map_v: K_nope (bf16) /
-// V (fp16) [B * lpad, 128 * 128]; map_kr: the rope keys [B * lpad, 64]. All boxes are 128 rows x 64
-// columns with the 128-byte swizzle.
-__global__ void __launch_bounds__(kPaThreads, 1)
+// map_qn: q_nope [T, 128 * 128] bf16 and map_qr: q_rope [T, 128 * 64], boxes of 128 rows; map_k: K_nope
+// [B * lpad, 128 * 128] bf16 and map_kr: the rope keys [B * lpad, 64], boxes of 64 rows; map_v: V (fp16)
+// [B * lpad, 128 * 128], boxes of 128 rows. Every box is 64 columns wide with the 128-byte swizzle.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPaThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap map_qn, const __grid_constant__ CUtensorMap map_qr,
                         const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                         const __grid_constant__ CUtensorMap map_kr, PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = sm;
-  uint8_t* kst0 = sm + kPaQBytes;                      // key tiles
-  uint8_t* vst0 = kst0 + kPaStages * kPaKBytes;        // value tiles
-  PaSmem* S = reinterpret_cast<PaSmem*>(vst0 + kPaStages * kPaVBytes);
+  uint8_t* kst0 = sm + kPaQBytes;                      // key tiles (this CTA's 64 keys)
+  uint8_t* vst0 = kst0 + kPaKStages * kPaKBytes;       // value tiles (this CTA's 64 columns)
+  PaSmem* S = reinterpret_cast<PaSmem*>(vst0 + kPaVStages * kPaVBytes);
+  const uint32_t rank = tc::cluster_ctarank();
+  const uint32_t cl = tc::cluster_id_x(), ncl = tc::n_clusters_x();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tc::mbar_init(&S->q_full, 1);
     tc::mbar_init(&S->q_empty, 1);
-    for (int s = 0; s < kPaStages; ++s) {
+    tc::mbar_init(&S->q_ready, 2);
+    for (int s = 0; s < kPaKStages; ++s) {
       tc::mbar_init(&S->k_full[s], 1);
       tc::mbar_init(&S->k_empty[s], 1);
+      tc::mbar_init(&S->k_ready[s], 2);
+    }
+    for (int s = 0; s < kPaVStages; ++s) {
       tc::mbar_init(&S->v_full[s], 1);
       tc::mbar_init(&S->v_empty[s], 1);
+      tc::mbar_init(&S->v_ready[s], 2);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&S->s_full[s], 1);
-      tc::mbar_init(&S->s_free[s], kPaSoftmaxWarps);
-      tc::mbar_init(&S->p_full[s], kPaSoftmaxWarps);
+      tc::mbar_init(&S->s_free[s], 2 * kPaSoftmaxWarps);
+      tc::mbar_init(&S->p_full[s], 2 * kPaSoftmaxWarps);
       tc::mbar_init(&S->o_done[s], 1);
     }
-    tc::mbar_init(&S->drain, 1);
+    tc::mbar_init(&S->drain[0], 1);
+    tc::mbar_init(&S->drain[1], 1);
     S->abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_map(&map_qn);
@@ -424,145 +453,208 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     tc::tma_prefetch_map(&map_v);
     tc::tma_prefetch_map(&map_kr);
   }
-  if (warp == kPaSoftmaxWarps + 1) tc::tmem_alloc<512>(&S->tmem_base);
+  if (warp == kPaSoftmaxWarps + 1) tc::tmem_alloc_pair<512>(&S->tmem_base);
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tm = S->tmem_base;
-  // K_nope and V come from the kv_up kernel ahead of this one
+  // K_nope, V and the rope keys come from the kv_up kernel ahead of this one
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int64_t n_units = static_cast<int64_t>(a.batch) * kH * a.qt_max;
+  const int64_t n_units = static_cast<int64_t>(a.batch) * kH * a.qp_max;
+  const int row_off = kPfRows * static_cast<int>(rank);   // this CTA's first row within the pair's 256
   if (warp == kPaSoftmaxWarps) {
-    // ------------------------------------------------------------ producer
-    // key tile g goes out as soon as the score MMA of tile g - 2 completed; value tile g - 1 after
-    // it (its PV comes after the softmax of tile g - 1), once the PV of tile g - 3 completed
+    // ------------------------------------------------------------ producer (both CTAs: own halves)
+    // key tile g goes out as soon as the score MMA of tile g - kPaKStages completed; value tile
+    // g - 1 after it, once the PV of tile g - 1 - kPaVStages completed
     if (lane == 0) {
       uint32_t n = 0, g = 0, gv = 0;   // units, key tiles and value tiles loaded
       int32_t pend_y = 0, pend_x = 0;  // value tile waiting to go out (when gv < g)
       bool ok = true;
       auto load_v = [&]() -> bool {
-        const int st = gv % kPaStages;
-        if (gv >= kPaStages && !tc::mbar_wait(&S->v_empty[st], ((gv / kPaStages) - 1) & 1)) return false;
-        uint8_t* dst = vst0 + st * kPaVBytes;
+        const int st = gv % kPaVStages;
+        if (gv >= kPaVStages && !tc::mbar_wait(&S->v_empty[st], ((gv / kPaVStages) - 1) & 1)) return false;
         tc::mbar_arrive_expect_tx(&S->v_full[st], kPaVBytes);
-        tc::tma_load_2d(dst, &map_v, pend_x, pend_y, &S->v_full[st]);
-        tc::tma_load_2d(dst + kPfBox, &map_v, pend_x + 64, pend_y, &S->v_full[st]);
+        tc::tma_load_2d(vst0 + st * kPaVBytes, &map_v, pend_x, pend_y, &S->v_full[st]);
         ++gv;
         return true;
       };
-      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int64_t u = cl; u < n_units && ok; u += ncl) {
         const PaUnit x = pa_unit(a, u);
         if (!x.live) continue;
         if (n > 0) ok = tc::mbar_wait(&S->q_empty, (n - 1) & 1);
         if (!ok || pa_aborted(S)) { ok = false; break; }
+        const int qrow = x.q0 + row_off;
         tc::mbar_arrive_expect_tx(&S->q_full, kPaQBytes);
-        tc::tma_load_2d(sQ, &map_qn, x.head * kDh, x.q0, &S->q_full);
-        tc::tma_load_2d(sQ + kPfBox, &map_qn, x.head * kDh + 64, x.q0, &S->q_full);
-        tc::tma_load_2d(sQ + 2 * kPfBox, &map_qr, x.head * kDr, x.q0, &S->q_full);
+        tc::tma_load_2d(sQ, &map_qn, x.head * kDh, qrow, &S->q_full);
+        tc::tma_load_2d(sQ + kPfBox, &map_qn, x.head * kDh + 64, qrow, &S->q_full);
+        tc::tma_load_2d(sQ + 2 * kPfBox, &map_qr, x.head * kDr, qrow, &S->q_full);
         ++n;
-        // the next unit's queries into L2 while this unit runs
-        for (int64_t w = u + gridDim.x; w < n_units; w += gridDim.x) {
-          const PaUnit y = pa_unit(a, w);
+        PaUnit y;   // this cluster's next unit: its queries and first tiles go to L2 early
+        y.live = false;
+        for (int64_t w = u + ncl; w < n_units; w += ncl) {
+          y = pa_unit(a, w);
           if (!y.live) continue;
-          pf_prefetch_2d(&map_qn, y.head * kDh, y.q0);
-          pf_prefetch_2d(&map_qn, y.head * kDh + 64, y.q0);
-          pf_prefetch_2d(&map_qr, y.head * kDr, y.q0);
+          pf_prefetch_2d(&map_qn, y.head * kDh, y.q0 + row_off);
+          pf_prefetch_2d(&map_qn, y.head * kDh + 64, y.q0 + row_off);
+          pf_prefetch_2d(&map_qr, y.head * kDr, y.q0 + row_off);
           break;
         }
+        auto l2_tile = [&](const PaUnit& z, int jj) {
+          const int64_t r0 = static_cast<int64_t>(z.b) * a.lpad + static_cast<int64_t>(jj) * kPfRows;
+          pf_prefetch_2d(&map_k, z.head * kDh, static_cast<int32_t>(r0 + 64 * rank));
+          pf_prefetch_2d(&map_k, z.head * kDh + 64, static_cast<int32_t>(r0 + 64 * rank));
+          pf_prefetch_2d(&map_kr, 0, static_cast<int32_t>(r0 + 64 * rank));
+          pf_prefetch_2d(&map_v, z.head * kDh + 64 * static_cast<int>(rank), static_cast<int32_t>(r0));
+        };
+        if (n == 1)
+          for (int jj = 0; jj < kPaL2Ahead && jj < x.nk; ++jj) l2_tile(x, jj);
         const int64_t krow0 = static_cast<int64_t>(x.b) * a.lpad;
         for (int j = 0; j < x.nk && ok; ++j, ++g) {
-          const int st = g % kPaStages;
-          if (g >= kPaStages) ok = tc::mbar_wait(&S->k_empty[st], ((g / kPaStages) - 1) & 1);
+          if (j + kPaL2Ahead < x.nk)
+            l2_tile(x, j + kPaL2Ahead);
+          else if (y.live && j + kPaL2Ahead - x.nk < y.nk)
+            l2_tile(y, j + kPaL2Ahead - x.nk);
+          const int st = g % kPaKStages;
+          if (g >= kPaKStages) ok = tc::mbar_wait(&S->k_empty[st], ((g / kPaKStages) - 1) & 1);
           if (!ok) break;
           uint8_t* kst = kst0 + st * kPaKBytes;
-          const int32_t yk = static_cast<int32_t>(krow0 + static_cast<int64_t>(j) * kPfRows);
+          const int32_t yk = static_cast<int32_t>(krow0 + static_cast<int64_t>(j) * kPfRows + 64 * rank);
           tc::mbar_arrive_expect_tx(&S->k_full[st], kPaKBytes);
           tc::tma_load_2d(kst, &map_k, x.head * kDh, yk, &S->k_full[st]);
-          tc::tma_load_2d(kst + kPfBox, &map_k, x.head * kDh + 64, yk, &S->k_full[st]);
-          tc::tma_load_2d(kst + 2 * kPfBox, &map_kr, 0, yk, &S->k_full[st]);
+          tc::tma_load_2d(kst + kPfHalfBox, &map_k, x.head * kDh + 64, yk, &S->k_full[st]);
+          tc::tma_load_2d(kst + 2 * kPfHalfBox, &map_kr, 0, yk, &S->k_full[st]);
           if (gv < g) ok = load_v();
-          pend_x = x.head * kDh;
-          pend_y = yk;
+          pend_x = x.head * kDh + 64 * static_cast<int>(rank);
+          pend_y = static_cast<int32_t>(krow0 + static_cast<int64_t>(j) * kPfRows);
         }
       }
       if (ok && gv < g) ok = load_v();
       if (!ok) pa_set_abort(S);
       if (n > 0) tc::mbar_wait(&S->q_full, (n - 1) & 1);
-      for (uint32_t q = g > kPaStages ? g - kPaStages : 0; q < g; ++q)
-        tc::mbar_wait(&S->k_full[q % kPaStages], (q / kPaStages) & 1);
-      for (uint32_t q = gv > kPaStages ? gv - kPaStages : 0; q < gv; ++q)
-        tc::mbar_wait(&S->v_full[q % kPaStages], (q / kPaStages) & 1);
+      for (uint32_t q = g > kPaKStages ? g - kPaKStages : 0; q < g; ++q)
+        tc::mbar_wait(&S->k_full[q % kPaKStages], (q / kPaKStages) & 1);
+      for (uint32_t q = gv > kPaVStages ? gv - kPaVStages : 0; q < gv; ++q)
+        tc::mbar_wait(&S->v_full[q % kPaVStages], (q / kPaVStages) & 1);
     }
-  } else if (warp == kPaSoftmaxWarps + 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kPaSoftmaxWarps + 2) {
+    // ------------------------------------------------------------ forwarder (both CTAs)
+    // tells the even CTA's MMA issuer when this CTA's queries, key half and value half have landed,
+    // in the order the producer requested them
     if (lane == 0) {
-      const uint32_t idesc_s = tc::idesc_bf16_f32(128, 128, 0, 0);
-      const uint32_t idesc_o = idesc_f16_f32(128, 128, 0, 1);
-      const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);         // K-major Q
-      const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(kst0), 16, 1024);       // K-major keys, stage 0
-      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(vst0), kPfBox, 1024);   // MN-major V, stage 0
-      uint32_t n = 0, g = 0;
+      const uint32_t q_ready0 = tc::map_peer(&S->q_ready, 0);
+      const uint32_t k_ready0 = tc::map_peer(&S->k_ready[0], 0);
+      const uint32_t v_ready0 = tc::map_peer(&S->v_ready[0], 0);
+      uint32_t n = 0, g = 0, gv = 0;
       bool ok = true;
-      // O (+)= P V of key tile gg (P from TMEM, 16 keys per MMA)
-      auto issue_pv = [&](uint32_t gg, bool first) -> bool {
-        const uint32_t s = gg & 1;
-        bool good = tc::mbar_wait(&S->v_full[gg % kPaStages], (gg / kPaStages) & 1);
-        if (good) good = tc::mbar_wait(&S->p_full[s], (gg >> 1) & 1);
-        if (!good || pa_aborted(S)) return false;
-        tc::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          tc::mma_ts(tm + kPaTmO, tm + kPaTmP + 64 * s + 8 * k,
-                     vdesc0 + static_cast<uint64_t>(((gg % kPaStages) * kPaVBytes + 2048 * k) >> 4), idesc_o,
-                     (first && k == 0) ? 0u : 1u);
-        tc::mma_commit(&S->o_done[s]);
-        tc::mma_commit(&S->v_empty[gg % kPaStages]);
+      auto fwd_v = [&]() -> bool {
+        const int st = gv % kPaVStages;
+        if (!tc::mbar_wait(&S->v_full[st], (gv / kPaVStages) & 1)) return false;
+        tc::mbar_arrive_cluster(v_ready0 + 8u * st);
+        ++gv;
         return true;
       };
-      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int64_t u = cl; u < n_units && ok; u += ncl) {
         const PaUnit x = pa_unit(a, u);
         if (!x.live) continue;
         ok = tc::mbar_wait(&S->q_full, n & 1);
+        if (!ok || pa_aborted(S)) { ok = false; break; }
+        tc::mbar_arrive_cluster(q_ready0);
+        ++n;
         for (int j = 0; j < x.nk && ok; ++j, ++g) {
-          const uint32_t s = g & 1;
-          ok = tc::mbar_wait(&S->k_full[g % kPaStages], (g / kPaStages) & 1);
+          const int st = g % kPaKStages;
+          ok = tc::mbar_wait(&S->k_full[st], (g / kPaKStages) & 1);
+          if (!ok || pa_aborted(S)) { ok = false; break; }
+          tc::mbar_arrive_cluster(k_ready0 + 8u * st);
+          if (gv < g) ok = fwd_v();
+        }
+      }
+      if (ok && gv < g) ok = fwd_v();
+      if (!ok) pa_set_abort(S);
+    }
+  } else if (warp == kPaSoftmaxWarps + 1) {
+    // ------------------------------------------------------------ score MMA issuer (even CTA)
+    // Scores and PVs go out from two threads, so that the tensor pipe stays fed while one of them
+    // waits for its next operands.
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc_s = tc::idesc_bf16_f32(256, 128, 0, 0);
+      const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);         // K-major Q, 128 rows
+      const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(kst0), 16, 1024);       // K-major keys, 64 rows
+      uint32_t n = 0, g = 0;
+      bool ok = true;
+      for (int64_t u = cl; u < n_units && ok; u += ncl) {
+        const PaUnit x = pa_unit(a, u);
+        if (!x.live) continue;
+        ok = tc::mbar_wait(&S->q_ready, n & 1);
+        for (int j = 0; j < x.nk && ok; ++j, ++g) {
+          const uint32_t s = g & 1, st = g % kPaKStages;
+          ok = tc::mbar_wait(&S->k_ready[st], (g / kPaKStages) & 1);
           if (ok && g >= 2) ok = tc::mbar_wait(&S->s_free[s], ((g - 2) >> 1) & 1);
           if (!ok || pa_aborted(S)) { ok = false; break; }
           tc::tc_fence_after();
-          const uint32_t kst = (g % kPaStages) * kPaKBytes;
 #pragma unroll
           for (int k = 0; k < 12; ++k) {
-            const uint32_t off = (k >> 2) * kPfBox + (k & 3) * 32;
-            tc::mma_ss(tm + kPaTmS + 128 * s, qdesc0 + static_cast<uint64_t>(off >> 4),
-                       kdesc0 + static_cast<uint64_t>((kst + off) >> 4), idesc_s, k > 0 ? 1u : 0u);
+            const uint32_t qoff = (k >> 2) * kPfBox + (k & 3) * 32;
+            const uint32_t koff = st * kPaKBytes + (k >> 2) * kPfHalfBox + (k & 3) * 32;
+            tc::mma_ss_pair(tm + kPaTmS + 128 * s, qdesc0 + static_cast<uint64_t>(qoff >> 4),
+                            kdesc0 + static_cast<uint64_t>(koff >> 4), idesc_s, k > 0 ? 1u : 0u);
           }
-          tc::mma_commit(&S->s_full[s]);
-          tc::mma_commit(&S->k_empty[g % kPaStages]);
-          if (j == x.nk - 1) tc::mma_commit(&S->q_empty);
-          if (j >= 1) ok = issue_pv(g - 1, j == 1);
+          tc::mma_commit_pair(&S->s_full[s]);
+          tc::mma_commit_pair(&S->k_empty[st]);
+          if (j == x.nk - 1) tc::mma_commit_pair(&S->q_empty);
         }
-        if (ok) ok = issue_pv(g - 1, x.nk == 1);
         ++n;
       }
       if (!ok) pa_set_abort(S);
-      tc::mma_commit(&S->drain);
-      tc::mbar_wait(&S->drain, 0);
+      tc::mma_commit_pair(&S->drain[0]);
+      tc::mbar_wait(&S->drain[0], 0);
+    }
+  } else if (warp == kPaSoftmaxWarps + 3) {
+    // ------------------------------------------------------------ PV MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc_o = idesc_f16_f32(256, 128, 0, 1);
+      const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(vst0), kPfBox, 1024);   // MN-major V, 64 columns
+      uint32_t g = 0;
+      bool ok = true;
+      for (int64_t u = cl; u < n_units && ok; u += ncl) {
+        const PaUnit x = pa_unit(a, u);
+        if (!x.live) continue;
+        for (int j = 0; j < x.nk && ok; ++j, ++g) {
+          // O (+)= P V of key tile g (P from TMEM, 16 keys per MMA); the first of a unit starts O afresh,
+          // after the softmax warps (whose P it waits for) have read the previous unit's O
+          const uint32_t s = g & 1, st = g % kPaVStages;
+          ok = tc::mbar_wait(&S->v_ready[st], (g / kPaVStages) & 1);
+          if (ok) ok = tc::mbar_wait(&S->p_full[s], (g >> 1) & 1);
+          if (!ok || pa_aborted(S)) { ok = false; break; }
+          tc::tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts_pair(tm + kPaTmO, tm + kPaTmP + 64 * s + 8 * k,
+                        vdesc0 + static_cast<uint64_t>((st * kPaVBytes + 2048 * k) >> 4), idesc_o,
+                        (j == 0 && k == 0) ? 0u : 1u);
+          tc::mma_commit_pair(&S->o_done[s]);
+          tc::mma_commit_pair(&S->v_empty[st]);
+        }
+      }
+      if (!ok) pa_set_abort(S);
+      tc::mma_commit_pair(&S->drain[1]);
+      tc::mbar_wait(&S->drain[1], 0);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-7)
-    // warp w: TMEM lane quarter w & 3 (query rows 32 (w & 3) .. + 31), key columns 64 (w >> 2) .. + 63
-    // of each tile and O columns 64 (w >> 2) .. + 63
+    // ------------------------------------------------------------ softmax (warps 0-7, both CTAs)
+    // warp w: TMEM lane quarter w & 3 (query rows 32 (w & 3) .. + 31 of this CTA), key columns
+    // 64 (w >> 2) .. + 63 of each tile and O columns 64 (w >> 2) .. + 63
     const int q4 = warp & 3, hc = warp >> 2;
     const int row = 32 * q4 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const uint32_t s_free0 = tc::map_peer(&S->s_free[0], 0), p_full0 = tc::map_peer(&S->p_full[0], 0);
     const float sl = a.scale_log2;
     uint32_t g = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int64_t u = cl; u < n_units && ok; u += ncl) {
       const PaUnit x = pa_unit(a, u);
       if (!x.live) continue;
-      const int qp = x.p0 + kPfRows * x.t + row;   // position of this row's token
+      const int qp = x.p0 + 2 * kPfRows * x.t + row_off + row;   // position of this row's token
       float m_used = -INFINITY, l = 0.f;
       // a wait that runs out stops this warp's waiting for the rest of the unit; the warps vote at
       // its end and leave together
@@ -585,7 +677,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         }
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&S->s_free[s]);
+        if (lane == 0) tc::mbar_arrive_cluster_relaxed(s_free0 + 8u * s);   // only TMEM was read
         // causal mask: key position k0 + i is visible to this row iff k0 + i <= qp
         const int k0 = kPfRows * j + 64 * hc;
         if (k0 + 63 > qp) {
@@ -645,7 +737,7 @@ __global__ void __launch_bounds__(kPaThreads, 1)
         }
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&S->p_full[s]);
+        if (lane == 0) tc::mbar_arrive_cluster(p_full0 + 8u * s);
       }
       // ---- epilogue: out = O / l for the rows that are this unit's tokens
       if (alive) alive = __all_sync(0xffffffffu, tc::mbar_wait(&S->o_done[(g - 1) & 1], ((g - 1) >> 1) & 1));
@@ -653,8 +745,8 @@ __global__ void __launch_bounds__(kPaThreads, 1)
       S->red_l[hc][row] = l;
       tc::named_sync(1 + q4, 64);
       const float inv = 1.f / (S->red_l[0][row] + S->red_l[1][row]);
-      const bool valid = kPfRows * x.t + row < x.n;
-      float* dst = a.out + (static_cast<int64_t>(x.q0 + row) * kH + x.head) * kDh + 64 * hc;
+      const bool valid = 2 * kPfRows * x.t + row_off + row < x.n;
+      float* dst = a.out + (static_cast<int64_t>(x.q0 + row_off + row) * kH + x.head) * kDh + 64 * hc;
       {
         uint32_t r0[32], r1[32];
         tc::tmem_ld32(tm + lane_base + kPaTmO + 64 * hc, r0);
@@ -676,11 +768,13 @@ __global__ void __launch_bounds__(kPaThreads, 1)
     }
     if (!ok) pa_set_abort(S);
   }
+  // ---------------------------------------------------------------- teardown
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc::tc_fence_before();
   __syncthreads();
+  tc::cluster_sync();   // no pair MMA, remote arrive or TMEM access of the other CTA is left
   tc::tc_fence_after();
-  if (warp == kPaSoftmaxWarps + 1) tc::tmem_dealloc<512>(tm);
+  if (warp == kPaSoftmaxWarps + 1) tc::tmem_dealloc_pair<512>(tm);
 }
 
 }  // namespace tcd
