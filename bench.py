@@ -151,9 +151,11 @@ class ClockSampler:
 
 # the sources a kernel is built from (paths relative to the repository root); a committed ncu
 # figure is used only while these files are unchanged
+_CSRC = "head_latent_attention_22_b300/csrc/"
 KERNEL_SOURCES = {
-    "attend_tc": ["head_latent_attention_22_b300/csrc/attend_pair.cuh", "head_latent_attention_22_b300/csrc/decode_tc.cuh",
-                  "head_latent_attention_22_b300/csrc/tc.cuh", "head_latent_attention_22_b300/csrc/common.cuh"],
+    "attend_tc": [_CSRC + "attend_pair.cuh", _CSRC + "decode_tc.cuh", _CSRC + "tc.cuh", _CSRC + "common.cuh"],
+    "prefill_attn": [_CSRC + "prefill.cuh", _CSRC + "decode_tc.cuh", _CSRC + "tc.cuh", _CSRC + "common.cuh"],
+    "kv_up": [_CSRC + "prefill.cuh", _CSRC + "decode_tc.cuh", _CSRC + "tc.cuh", _CSRC + "common.cuh"],
 }
 
 
