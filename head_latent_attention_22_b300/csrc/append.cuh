@@ -13,12 +13,16 @@ namespace mla {
 // "NTK-by-parts" rule of YaRN (Peng et al. 2023) that the DeepSeek-V2 report applies
 // (section 3.1.4): a pair making r = orig_len f / (2 pi) turns over the original context
 // keeps f for r >= beta, takes f / s for r <= alpha, and blends linearly in r between.
+constexpr int kRopeTable = 64;   // pairs whose frequency the host computes (d_rope <= 128)
+
 struct RopeFreq {
   double log_theta;
   double yarn_s, yarn_alpha, yarn_beta, yarn_orig_len;   // yarn_s <= 1: plain RoPE
+  int n_table;                                           // pairs m < n_table take table[m]
+  double table[kRopeTable];                              // f_m, computed by the host by the rule below
 };
 
-__device__ __forceinline__ double rope_freq(const RopeFreq& r, int m, int d_rope) {
+__host__ __device__ inline double rope_freq_rule(const RopeFreq& r, int m, int d_rope) {
   double f = exp(-(2.0 * m / d_rope) * r.log_theta);
   if (r.yarn_s > 1.0) {
     const double turns = r.yarn_orig_len * f / (2.0 * 3.141592653589793);
@@ -27,6 +31,10 @@ __device__ __forceinline__ double rope_freq(const RopeFreq& r, int m, int d_rope
     f = (1.0 - g) * f / r.yarn_s + g * f;
   }
   return f;
+}
+
+__device__ __forceinline__ double rope_freq(const RopeFreq& r, int m, int d_rope) {
+  return m < r.n_table ? r.table[m] : rope_freq_rule(r, m, d_rope);
 }
 
 struct AppendArgs {
@@ -58,12 +66,30 @@ __device__ __forceinline__ int64_t append_slot(const AppendArgs& a, int t, int* 
   return page * a.page_size + pos % a.page_size;
 }
 
-// Rotation of pair m at position pos: angle pos * f_m in fp64.
+// Rotation of pair m at position pos by the angle pos * f_m, formed in fp64. For a result stored in
+// bf16 (kBf16Out) the angle is reduced to [-pi, pi] in fp64 (Cody-Waite reduction by 2 pi split into
+// a head and a tail) and its sine and cosine are taken in fp32: their error (a few 1e-8) is far
+// below the bf16 rounding of the stored value, while fp64 sines and cosines are slow on this part.
+// A result stored in fp32 keeps the fp64 sine and cosine.
+template <bool kBf16Out>
 __device__ __forceinline__ void rope_pair(double a, double b, int m, int d_rope, int pos,
                                           const RopeFreq& rf, double* ra, double* rb) {
   const double inv_freq = rope_freq(rf, m, d_rope);
-  double sn, cs;
-  sincos(static_cast<double>(pos) * inv_freq, &sn, &cs);
+  const double ang = static_cast<double>(pos) * inv_freq;
+  if (!kBf16Out) {
+    double sn, cs;
+    sincos(ang, &sn, &cs);
+    *ra = a * cs - b * sn;
+    *rb = a * sn + b * cs;
+    return;
+  }
+  constexpr double kTwoPiHi = 6.283185307179586;          // 2 pi rounded to fp64
+  constexpr double kTwoPiLo = 2.4492935982947064e-16;     // 2 pi - kTwoPiHi
+  const double k = rint(ang * (1.0 / kTwoPiHi));
+  const double red = fma(-k, kTwoPiLo, fma(-k, kTwoPiHi, ang));
+  float sf, cf;
+  sincosf(static_cast<float>(red), &sf, &cf);
+  const double sn = sf, cs = cf;
   *ra = a * cs - b * sn;
   *rb = a * sn + b * cs;
 }
@@ -151,7 +177,7 @@ __global__ void __launch_bounds__(256) append_dsv2_kernel(AppendArgs a) {
   const int i0 = a.rope_interleaved ? 2 * lane : lane;
   const int i1 = a.rope_interleaved ? 2 * lane + 1 : lane + 32;
   double ra, rb;
-  rope_pair(bf16_to_f32(kr[i0]), bf16_to_f32(kr[i1]), lane, 64, pos, a.rf, &ra, &rb);
+  rope_pair<true>(bf16_to_f32(kr[i0]), bf16_to_f32(kr[i1]), lane, 64, pos, a.rf, &ra, &rb);
   if (a.rope_interleaved) {
     *reinterpret_cast<uint32_t*>(kdst + i0) =
         static_cast<uint32_t>(f64_to_bf16_bits(ra)) | (static_cast<uint32_t>(f64_to_bf16_bits(rb)) << 16);
@@ -215,7 +241,10 @@ __global__ void __launch_bounds__(256) append_generic_kernel(AppendArgs a) {
     const int i0 = a.rope_interleaved ? 2 * m : m;
     const int i1 = a.rope_interleaved ? 2 * m + 1 : m + half;
     double ra, rb;
-    rope_pair(load_as_f32(k, i0), load_as_f32(k, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
+    if (a.cache_dtype == MLA_DTYPE_FP32)
+      rope_pair<false>(load_as_f32(k, i0), load_as_f32(k, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
+    else
+      rope_pair<true>(load_as_f32(k, i0), load_as_f32(k, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
     if (a.cache_dtype == MLA_DTYPE_FP32) {
       float* dst = reinterpret_cast<float*>(row + rope_off);
       dst[i0] = static_cast<float>(ra);
@@ -257,7 +286,7 @@ __global__ void rope_query_kernel(RopeQueryArgs a) {
     const T* src = static_cast<const T*>(a.in) + row * a.d_rope;
     T* dst = static_cast<T*>(a.out) + row * a.d_rope;
     double ra, rb;
-    rope_pair(load_as_f32(src, i0), load_as_f32(src, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
+    rope_pair<sizeof(T) == 2>(load_as_f32(src, i0), load_as_f32(src, i1), m, a.d_rope, pos, a.rf, &ra, &rb);
     if constexpr (sizeof(T) == 4) {
       dst[i0] = static_cast<float>(ra);
       dst[i1] = static_cast<float>(rb);

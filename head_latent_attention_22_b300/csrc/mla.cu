@@ -82,6 +82,11 @@ RopeFreq rope_freq_of(const mla_config* c) {
     r.yarn_beta = c->yarn_beta;
     r.yarn_orig_len = c->yarn_orig_len;
   }
+  r.n_table = 0;
+  if (c->d_rope / 2 <= kRopeTable) {
+    for (int m = 0; m < c->d_rope / 2; ++m) r.table[m] = rope_freq_rule(r, m, c->d_rope);
+    r.n_table = c->d_rope / 2;
+  }
   return r;
 }
 
