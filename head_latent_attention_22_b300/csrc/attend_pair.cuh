@@ -49,6 +49,7 @@ constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 12
 constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
 constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
 constexpr int kPrEarlyBatch = 1024;                 // largest batch whose first tiles load before the plan is read
+constexpr int kPrF8Ahead = 8;                       // FP8 cache: tiles prefetched to L2 ahead of their loads
 
 struct PairSmem {
   uint64_t full[kPrMaxStages];    // this CTA's half of a tile landed (TMA; bf16 cache)
@@ -103,8 +104,10 @@ __device__ __forceinline__ void pr_set_abort(PairSmem* s) {
 //   map_rope:  the rope values as bf16 [rows, 64] (row stride 656 bytes), boxes of 64 x 32, 64-byte swizzle.
 // map_q:  Q_lat row-major [B * 128 heads, 576] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle.
 // map_qr: the same Q_lat, boxes of 16 rows x 32 columns, 64-byte swizzle.
-// The FP8 codes are dequantised (code x block scale, rounded to bf16) by four extra warps into the
-// same bf16 tile layout a bf16 pool gives, so the MMAs and the softmax do not depend on the format.
+// The FP8 codes are dequantised by four extra warps into the tile layout a bf16 pool gives, in fp16
+// (code x block scale: the code converts exactly, one packed fp16 multiply): fp16 keeps 3 more bits
+// than bf16 and costs two instructions per pair of values. The latent part of the queries (written
+// by the absorb kernel) and P are then fp16 too; the rope part stays bf16 with its own MMA kind.
 template <bool kF8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThreads, 1)
     attend_pair_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_rope,
@@ -261,8 +264,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
         const int jl = jc + lane;
         if (jl < j1) y_l = tile_row(b, jl);
         const int n = min(32, j1 - jc);
+        // FP8 cache: the raw ring is two tiles deep, less than HBM's latency at this tile rate, so
+        // tiles go to L2 kPrF8Ahead tiles before their loads
+        auto l2_tile = [&](int32_t yy) {
+          tc::tma_prefetch_l2_2d(&map_lat, static_cast<int>(rank) * 256, yy);
+          tc::tma_prefetch_l2_2d(&map_scale, kDc, yy);
+          tc::tma_prefetch_l2_2d(&map_rope, 32 * static_cast<int>(rank), yy);
+        };
+        if (kF8 && lane < kPrF8Ahead && lane < n) l2_tile(y_l);
         for (int u = 0; u < n; ++u) {
           const int32_t y = __shfl_sync(0xffffffffu, y_l, u);
+          const int32_t y_ahead = __shfl_sync(0xffffffffu, y_l, (u + kPrF8Ahead) & 31);
+          if (kF8 && lane == 0 && u + kPrF8Ahead < n) l2_tile(y_ahead);
           if (lane == 0 && ok && it >= n_pre) {   // tiles before n_pre went out before the wait
             const int st = it % kPrStages;
             if (it >= kPrStages) ok = tc::mbar_wait(&S->empty[st], ((it / kPrStages) - 1) & 1);
@@ -295,7 +308,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
     // from a third: the tensor pipe stays fed while one thread waits or loops.
     if (rank == 0 && lane == 0) {
       const uint32_t mine = warp == 1 ? 0u : 1u;   // tile parity this thread issues
-      const uint32_t idesc_s = tc::idesc_bf16_f32(256, 128, 0, 0);
+      const uint32_t idesc_s = tc::idesc_bf16_f32(256, 128, 0, 0);                // rope part: bf16
+      // latent part: bf16, or fp16 (A and B format fields 0) with an FP8 cache
+      const uint32_t idesc_l = kF8 ? ((1u << 4) | ((128u >> 3) << 17) | ((256u >> 4) << 24)) : idesc_s;
       const uint64_t qdesc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);       // K-major Q, 128 rows
       const uint64_t kdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), 16, 1024);   // K-major tile, 64 rows
       const uint64_t qrdesc0 = tc::sdesc_sw64(tc::smem_u32(sQ + 4 * kPrQBox), 16, 512);        // rope part of Q
@@ -319,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
             const int box = k >> 2, off = (k & 3) * 32;
             const uint64_t ad = qdesc0 + static_cast<uint64_t>((box * kPrQBox + off) >> 4);
             const uint64_t bd = kdesc0 + static_cast<uint64_t>((st * kPrStageBytes + box * kPrBox + off) >> 4);
-            tc::mma_ss_pair(d, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+            tc::mma_ss_pair(d, ad, bd, idesc_l, k > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int k = 0; k < kPrKSteps - 16; ++k) {
@@ -341,7 +356,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
   } else if (warp == 2) {
     // ---------------------------------------------------------------- PV MMA issuer (even CTA)
     if (rank == 0 && lane == 0) {
-      const uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+      // P x V: bf16, or fp16 with an FP8 cache
+      const uint32_t idesc_o =
+          kF8 ? ((1u << 4) | (1u << 16) | ((256u >> 3) << 17) | ((128u >> 4) << 24)) : tc::idesc_bf16_f32(128, 256, 0, 1);
       const uint64_t vdesc0 = tc::sdesc_sw128(tc::smem_u32(stages), kPrBox, 1024);   // MN-major V
       const uint64_t plo0 = tc::sdesc_sw64(tc::smem_u32(stages + 4 * kPrBox), 16, 512);   // P tokens 0..31, stage 0
       const uint64_t phi0 = tc::sdesc_sw64(tc::smem_u32(sP), 16, 512);                    // P tokens 32..63, buffer 0
@@ -441,6 +458,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
         const int row = ci >> 5, k = ci & 31;   // chunk k = latent 8k .. 8k + 7 of this CTA's 256
         const uint2 codes = *reinterpret_cast<const uint2*>(raw + row * 256 + 8 * k);
         const float sc = reinterpret_cast<const float*>(raw + CF::kRawCodes + row * 16)[2 * rank + (k >> 4)];
+        uint32_t sc2;   // the block scale in both halves of an fp16 pair
+        asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(sc2) : "f"(sc));
         const uint32_t cw[2] = {codes.x, codes.y};
         uint32_t o[4];
 #pragma unroll
@@ -448,8 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
           const uint16_t pair = static_cast<uint16_t>(cw[i >> 1] >> (16 * (i & 1)));
           uint32_t h2;
           asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-          const float2 v = add_f16x2_f32(h2, 0u);
-          o[i] = tc::pack_bf16(v.x * sc, v.y * sc);
+          asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(h2), "r"(sc2));
         }
         *reinterpret_cast<uint4*>(stage + (k >> 3) * kPrBox + row * 128 + (((k & 7) ^ (row & 7)) << 4)) =
             make_uint4(o[0], o[1], o[2], o[3]);
@@ -542,10 +560,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
         float ps[2] = {0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint32_t w = tc::pack_bf16(tc::ex2_approx(fmaf(s[2 * c], sl, neg_m)),
-                                           tc::ex2_approx(fmaf(s[2 * c + 1], sl, neg_m)));
-          p[c] = w;
-          ps[c & 1] += bf_lo(w) + bf_hi(w);
+          const float e0 = tc::ex2_approx(fmaf(s[2 * c], sl, neg_m)), e1 = tc::ex2_approx(fmaf(s[2 * c + 1], sl, neg_m));
+          // l sums the values the PV multiplies: P after its rounding to the MMA type
+          if (kF8) {
+            const __half2 h = __floats2half2_rn(e0, e1);
+            p[c] = *reinterpret_cast<const uint32_t*>(&h);
+            const float2 f = __half22float2(h);
+            ps[c & 1] += f.x + f.y;
+          } else {
+            const uint32_t w = tc::pack_bf16(e0, e1);
+            p[c] = w;
+            ps[c & 1] += bf_lo(w) + bf_hi(w);
+          }
         }
         l += ps[0] + ps[1];
         if (lane < 16) S->alpha[it & 1][hl] = alpha;

@@ -66,6 +66,7 @@ struct AbsorbArgs {
   uint16_t* q_lat;            // row-major [B, H, 576], see qlat_row_index
   Plan plan;
   int batch, nb, max_seq_len, ncl;
+  int f16_lat;                // 1: the latent part of Q_lat in fp16 (the operand type of an FP8 cache's tiles)
 };
 
 __host__ __device__ __forceinline__ int64_t qlat_row_index(int64_t b, int head, int k) {
@@ -222,7 +223,8 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
           const int b = n0 + c0 + c;
           const int k = 256 * half + mt * 128 + 32 * warp + lane;   // latent element
           if (b < a.batch && ok)
-            a.q_lat[qlat_row_index(b, i, k)] = f32_to_bf16_bits(__uint_as_float(r[c]));
+            a.q_lat[qlat_row_index(b, i, k)] =
+                a.f16_lat ? __half_as_ushort(__float2half_rn(__uint_as_float(r[c]))) : f32_to_bf16_bits(__uint_as_float(r[c]));
         }
       }
     }

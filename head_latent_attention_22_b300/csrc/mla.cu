@@ -443,6 +443,7 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   aa.nb = p.nb;
   aa.max_seq_len = max_seq_len;
   aa.ncl = ncl;
+  aa.f16_lat = f8 ? 1 : 0;
 
   tcd::AttendArgs ta{};
   ta.q_lat = q_lat;
