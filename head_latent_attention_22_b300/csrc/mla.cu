@@ -589,8 +589,8 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
   const uint64_t wkv = static_cast<uint64_t>(tcd::kH) * tcd::kDh;
   CUtensorMap m_lat, m_wuk, m_wuv, m_qn, m_qr, m_k, m_v, m_kr;
   if (!make_map_2d(&m_lat, pool, BF, tcd::kRow, static_cast<uint64_t>(pool_rows), tcd::kRow * 2, 64, 64, SW) ||
-      !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt, SW) ||
-      !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt, SW) ||
+      !make_map_2d(&m_wuk, w_uk, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt / 2, SW) ||
+      !make_map_2d(&m_wuv, w_uv, BF, tcd::kDc, wkv, tcd::kDc * 2, 64, tcd::kKvNt / 2, SW) ||
       !make_map_2d(&m_qn, q_nope, BF, wkv, static_cast<uint64_t>(n_tokens), wkv * 2, 64, tcd::kPfRows, SW) ||
       !make_map_2d(&m_qr, q_rope, BF, static_cast<uint64_t>(tcd::kH) * tcd::kDr, static_cast<uint64_t>(n_tokens),
                    static_cast<uint64_t>(tcd::kH) * tcd::kDr * 2, 64, tcd::kPfRows, SW) ||
@@ -630,8 +630,12 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
   pa.scale_log2 = softmax_scale(c) * 1.4426950408889634f;
 
   const int sms = current_sm_count();
-  const int64_t items = static_cast<int64_t>(p.lpad / tcd::kPfRows) * batch * tcd::kKvGroups;
-  const int g_kv = static_cast<int>(items < sms ? items : sms);
+  const int64_t items = ((static_cast<int64_t>(p.lpad / tcd::kPfRows) * batch + 1) / 2) * tcd::kKvGroups;
+  int kv_clusters = 0;
+  mla_status ks = cluster_count(reinterpret_cast<const void*>(tcd::kv_up_kernel), tcd::kKvThreads, tcd::kKvSmem,
+                                &kv_clusters);
+  if (ks != MLA_OK) return ks;
+  if (items < kv_clusters) kv_clusters = static_cast<int>(items);
   const int64_t units = static_cast<int64_t>(batch) * tcd::kH * pa.qp_max;
   int pa_clusters = 0;
   mla_status cs = cluster_count(reinterpret_cast<const void*>(tcd::prefill_attn_kernel), tcd::kPaThreads, tcd::kPaSmem,
@@ -640,8 +644,8 @@ mla_status prefill_tc(const mla_config* c, const void* q_nope, const void* q_rop
   if (units < pa_clusters) pa_clusters = static_cast<int>(units);
   stage_mark(0, st);
   void* kv_args[] = {&m_lat, &m_wuk, &m_wuv, &ka};
-  mla_status s = launch_pdl(reinterpret_cast<const void*>(tcd::kv_up_kernel), dim3(g_kv), dim3(tcd::kKvThreads),
-                            tcd::kKvSmem, st, kv_args);
+  mla_status s = launch_pdl(reinterpret_cast<const void*>(tcd::kv_up_kernel), dim3(2 * kv_clusters),
+                            dim3(tcd::kKvThreads), tcd::kKvSmem, st, kv_args);
   if (s != MLA_OK) return s;
   stage_mark(1, st);
   void* pa_args[] = {&m_qn, &m_qr, &m_k, &m_v, &m_kr, &pa};

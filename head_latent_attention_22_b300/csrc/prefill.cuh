@@ -13,11 +13,11 @@
 // whose scores have the contraction width d_h + d_h^R = 192 instead of the
 // 576 of the absorbed form the decode uses.
 //
-//   kv_up_kernel:        [rows x 512] latent tile (gathered from the pages) x
+//   kv_up_kernel:        [rows x 512] latent tiles (gathered from the pages) x
 //                        [W_UK ; W_UV]^T ([512 x 32768]) -> K_nope (bf16, the
 //                        query's type, for the score MMA) and V (fp16)
-//                        [B * L_pad, 128 heads x 128]. tcgen05 MMA
-//                        M = 128 rows, N = 256, K = 16; fp32 accumulators in
+//                        [B * L_pad, 128 heads x 128]. Pair MMAs on two CTAs
+//                        (M = 256 rows, N = 256, K = 16); fp32 accumulators in
 //                        TMEM, two of them so the epilogue of one column
 //                        tile overlaps the MMAs of the next.
 //   prefill_attn_kernel: per (sequence, head, 256 query rows) on a CTA pair:
@@ -66,17 +66,21 @@ constexpr int kPfHalfBox = 64 * 128;      // 64 rows x 64 bf16 = 8 KB
 constexpr int kPfWidthKV = 2 * kH * kDh;  // columns of [K_nope | V] per token: 32768
 
 // ------------------------------------------------------------------ kv_up_kernel
-constexpr int kKvNt = 256;                            // weight rows (output columns) per MMA tile
+// A cluster of two CTAs computes two 128-row tiles (CTA r: row tile 2 p + r) against the same
+// 256 weight rows with pair MMAs (M = 256, N = 256): each CTA streams only its 128 of the 256 weight
+// rows, 16 KB per 64-column chunk where a CTA working alone would stream 32 KB; the weight stream
+// is what one SM's tensor-memory-access unit (about 34 bytes per cycle) could not keep up with.
+constexpr int kKvNt = 256;                            // weight rows (output columns) per pair MMA tile
 constexpr int kKvTilesPerItem = 16;                   // column tiles a work item covers
-constexpr int kKvGroups = kPfWidthKV / kKvNt / kKvTilesPerItem;   // 8 items per row tile
-constexpr int kKvStages = 3;                          // weight chunk ring: 256 rows x 64 columns = 32 KB each
+constexpr int kKvGroups = kPfWidthKV / kKvNt / kKvTilesPerItem;   // 8 items per pair of row tiles
+constexpr int kKvStages = 4;                          // weight chunk ring: 128 rows x 64 columns = 16 KB each
 constexpr int kKvABytes = 8 * kPfBox;                 // latent tile: 8 boxes of 128 rows x 64 columns = 128 KB
-constexpr int kKvBBytes = kKvNt * 128;                // 32 KB
-constexpr int kKvThreads = 32 * 6;                    // producer, MMA, 4 epilogue warps
+constexpr int kKvBBytes = (kKvNt / 2) * 128;          // 16 KB
+constexpr int kKvThreads = 32 * 7;                    // producer, MMA issuer, 4 epilogue warps, forwarder
 
 struct KvUpSmem {
-  uint64_t a_full, a_empty;
-  uint64_t b_full[kKvStages], b_empty[kKvStages];
+  uint64_t a_full, a_empty, a_ready;
+  uint64_t b_full[kKvStages], b_empty[kKvStages], b_ready[kKvStages];
   uint64_t d_full[2], d_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -120,26 +124,41 @@ __device__ __forceinline__ bool kv_aborted(const KvUpSmem* s) {
 }
 __device__ __forceinline__ void kv_set_abort(KvUpSmem* s) { *reinterpret_cast<volatile int32_t*>(&s->abort_flag) = 1; }
 
-// Work item i: row tile r of sequence b, column tiles [16 g, 16 g + 16). Items whose rows lie past
-// the sequence's length are empty.
+// Work item i: row tiles 2 p and 2 p + 1 (row tile t: rows 128 (t / B) .. of sequence t mod B),
+// column tiles [16 g, 16 g + 16). A row tile past its sequence's length is dead: its CTA still takes
+// part in the pair MMAs (its half of the weights) but loads zeros and writes nothing; an item whose
+// two tiles are both dead is skipped.
 struct KvItem {
   int b, r, g;
-  bool live;
+  bool live, any;
 };
-__device__ __forceinline__ KvItem kv_item(const KvUpArgs& a, int64_t i) {
+__device__ __forceinline__ KvItem kv_item(const KvUpArgs& a, int64_t i, uint32_t rank) {
+  const int64_t n_rt = static_cast<int64_t>(a.batch) * (a.lpad / kPfRows);
   KvItem it;
   it.g = static_cast<int>(i % kKvGroups);
-  const int64_t rb = i / kKvGroups;
-  it.b = static_cast<int>(rb % a.batch);
-  it.r = static_cast<int>(rb / a.batch);
-  const int L = clamp_len(a.seq_lens[it.b], a.max_seq_len);
-  it.live = static_cast<int64_t>(it.r) * kPfRows < L;
+  const int64_t p = i / kKvGroups;
+  it.any = false;
+  it.b = 0;
+  it.r = 0;
+  it.live = false;
+  for (uint32_t q = 0; q < 2; ++q) {
+    const int64_t rt = 2 * p + q;
+    if (rt >= n_rt) continue;
+    const int b = static_cast<int>(rt % a.batch), r = static_cast<int>(rt / a.batch);
+    const bool lv = static_cast<int64_t>(r) * kPfRows < clamp_len(a.seq_lens[b], a.max_seq_len);
+    it.any = it.any || lv;
+    if (q == rank) {
+      it.b = b;
+      it.r = r;
+      it.live = lv;
+    }
+  }
   return it;
 }
 
 // map_lat: the pool [rows, 576] bf16, boxes of 64 rows x 64 columns, 128-byte swizzle.
-// map_wuk / map_wuv: W_UK / W_UV as [128 * 128, 512] bf16, boxes of 256 rows x 64 columns.
-__global__ void __launch_bounds__(kKvThreads, 1)
+// map_wuk / map_wuv: W_UK / W_UV as [128 * 128, 512] bf16, boxes of 128 rows x 64 columns.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     kv_up_kernel(const __grid_constant__ CUtensorMap map_lat, const __grid_constant__ CUtensorMap map_wuk,
                  const __grid_constant__ CUtensorMap map_wuv, KvUpArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -147,17 +166,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   uint8_t* sA = sm;
   uint8_t* sB = sm + kKvABytes;
   KvUpSmem* S = reinterpret_cast<KvUpSmem*>(sB + kKvStages * kKvBBytes);
+  const uint32_t rank = tc::cluster_ctarank();
+  const uint32_t cl = tc::cluster_id_x(), ncl = tc::n_clusters_x();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tc::mbar_init(&S->a_full, 1);
     tc::mbar_init(&S->a_empty, 1);
+    tc::mbar_init(&S->a_ready, 2);
     for (int s = 0; s < kKvStages; ++s) {
       tc::mbar_init(&S->b_full[s], 1);
       tc::mbar_init(&S->b_empty[s], 1);
+      tc::mbar_init(&S->b_ready[s], 2);
     }
     for (int d = 0; d < 2; ++d) {
       tc::mbar_init(&S->d_full[d], 1);
-      tc::mbar_init(&S->d_free[d], 4);
+      tc::mbar_init(&S->d_free[d], 8);   // the 4 epilogue warps of both CTAs
     }
     tc::mbar_init(&S->drain, 1);
     S->abort_flag = 0;
@@ -166,26 +189,26 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     tc::tma_prefetch_map(&map_wuk);
     tc::tma_prefetch_map(&map_wuv);
   }
-  if (warp == 1) tc::tmem_alloc<512>(&S->tmem_base);
+  if (warp == 1) tc::tmem_alloc_pair<512>(&S->tmem_base);
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tm = S->tmem_base;
   // the pool rows and the lengths come from the kernels ahead of this one on the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int64_t n_items = static_cast<int64_t>((a.lpad / kPfRows)) * a.batch * kKvGroups;
+  const int64_t n_items = ((static_cast<int64_t>(a.lpad / kPfRows) * a.batch + 1) / 2) * kKvGroups;
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs: own tile, own weight half)
     if (lane == 0) {
       uint32_t n = 0, c = 0;   // items and weight chunks loaded
       bool ok = true;
-      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-        const KvItem it = kv_item(a, i);
-        if (!it.live) continue;
+      for (int64_t i = cl; i < n_items && ok; i += ncl) {
+        const KvItem it = kv_item(a, i, rank);
+        if (!it.any) continue;
         if (n > 0) ok = tc::mbar_wait(&S->a_empty, (n - 1) & 1);
         if (!ok || kv_aborted(S)) { ok = false; break; }
-        const int L = clamp_len(a.seq_lens[it.b], a.max_seq_len);
+        const int L = it.live ? clamp_len(a.seq_lens[it.b], a.max_seq_len) : 0;
         tc::mbar_arrive_expect_tx(&S->a_full, kKvABytes);
         for (int h = 0; h < 2; ++h) {
           const int64_t tok = static_cast<int64_t>(it.r) * kPfRows + 64 * h;
@@ -195,7 +218,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         ++n;
         for (int t = 0; t < kKvTilesPerItem && ok; ++t) {
-          const int n0 = (it.g * kKvTilesPerItem + t) * kKvNt;
+          const int n0 = (it.g * kKvTilesPerItem + t) * kKvNt + (kKvNt / 2) * static_cast<int>(rank);
           const CUtensorMap* mw = n0 < kH * kDh ? &map_wuk : &map_wuv;
           const int row = n0 < kH * kDh ? n0 : n0 - kH * kDh;
           for (int kc = 0; kc < 8; ++kc, ++c) {
@@ -213,55 +236,81 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const uint32_t first = c > kKvStages ? c - kKvStages : 0;
       for (uint32_t q = first; q < c; ++q) tc::mbar_wait(&S->b_full[q % kKvStages], (q / kKvStages) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ forwarder (both CTAs)
+    // tells the even CTA's MMA issuer when this CTA's tile and weight chunks have landed, in the
+    // order the producer requested them
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(128, kKvNt, 0, 0);
+      const uint32_t a_ready0 = tc::map_peer(&S->a_ready, 0);
+      const uint32_t b_ready0 = tc::map_peer(&S->b_ready[0], 0);
+      uint32_t n = 0, c = 0;
+      bool ok = true;
+      for (int64_t i = cl; i < n_items && ok; i += ncl) {
+        const KvItem it = kv_item(a, i, rank);
+        if (!it.any) continue;
+        ok = tc::mbar_wait(&S->a_full, n & 1);
+        if (!ok || kv_aborted(S)) { ok = false; break; }
+        tc::mbar_arrive_cluster(a_ready0);
+        ++n;
+        for (int q = 0; q < kKvTilesPerItem * 8 && ok; ++q, ++c) {
+          const int st = c % kKvStages;
+          ok = tc::mbar_wait(&S->b_full[st], (c / kKvStages) & 1);
+          if (!ok || kv_aborted(S)) { ok = false; break; }
+          tc::mbar_arrive_cluster(b_ready0 + 8u * st);
+        }
+      }
+      if (!ok) kv_set_abort(S);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(256, kKvNt, 0, 0);
       const uint64_t adesc0 = tc::sdesc_sw128(tc::smem_u32(sA), 16, 1024);
       const uint64_t bdesc0 = tc::sdesc_sw128(tc::smem_u32(sB), 16, 1024);
       uint32_t n = 0, c = 0, d = 0;   // items, weight chunks, column tiles
       bool ok = true;
-      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-        const KvItem it = kv_item(a, i);
-        if (!it.live) continue;
-        ok = tc::mbar_wait(&S->a_full, n & 1);
+      for (int64_t i = cl; i < n_items && ok; i += ncl) {
+        const KvItem it = kv_item(a, i, rank);
+        if (!it.any) continue;
+        ok = tc::mbar_wait(&S->a_ready, n & 1);
         for (int t = 0; t < kKvTilesPerItem && ok; ++t, ++d) {
           const uint32_t buf = d & 1;
           if (d >= 2) ok = tc::mbar_wait(&S->d_free[buf], ((d >> 1) - 1) & 1);
           for (int kc = 0; kc < 8 && ok; ++kc, ++c) {
             const int st = c % kKvStages;
-            ok = tc::mbar_wait(&S->b_full[st], (c / kKvStages) & 1);
+            ok = tc::mbar_wait(&S->b_ready[st], (c / kKvStages) & 1);
             if (!ok || kv_aborted(S)) { ok = false; break; }
             tc::tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              tc::mma_ss(tm + 256 * buf, adesc0 + static_cast<uint64_t>((kc * kPfBox + 32 * k) >> 4),
-                         bdesc0 + static_cast<uint64_t>((st * kKvBBytes + 32 * k) >> 4), idesc,
-                         (kc == 0 && k == 0) ? 0u : 1u);
-            tc::mma_commit(&S->b_empty[st]);
+              tc::mma_ss_pair(tm + 256 * buf, adesc0 + static_cast<uint64_t>((kc * kPfBox + 32 * k) >> 4),
+                              bdesc0 + static_cast<uint64_t>((st * kKvBBytes + 32 * k) >> 4), idesc,
+                              (kc == 0 && k == 0) ? 0u : 1u);
+            tc::mma_commit_pair(&S->b_empty[st]);
           }
-          if (ok) tc::mma_commit(&S->d_full[buf]);
+          if (ok) tc::mma_commit_pair(&S->d_full[buf]);
         }
-        if (ok) tc::mma_commit(&S->a_empty);
+        if (ok) tc::mma_commit_pair(&S->a_empty);
         ++n;
       }
       if (!ok) kv_set_abort(S);
-      tc::mma_commit(&S->drain);
+      tc::mma_commit_pair(&S->drain);
       tc::mbar_wait(&S->drain, 0);
     }
   } else {
-    // ------------------------------------------------------------ epilogue: TMEM -> bf16 rows of K_nope / V
+    // ------------------------------------------------------------ epilogue (both CTAs): TMEM -> K_nope / V rows
     const int q = warp & 3;   // TMEM lane quarter of this warp
     const int row = 32 * q + lane;
+    const uint32_t d_free0 = tc::map_peer(&S->d_free[0], 0);
     uint32_t d = 0;
     bool ok = true;
-    for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const KvItem it = kv_item(a, i);
-      if (!it.live) continue;
-      const int L = clamp_len(a.seq_lens[it.b], a.max_seq_len);
+    for (int64_t i = cl; i < n_items && ok; i += ncl) {
+      const KvItem it = kv_item(a, i, rank);
+      if (!it.any) continue;
+      const int L = it.live ? clamp_len(a.seq_lens[it.b], a.max_seq_len) : 0;
       const bool valid = static_cast<int64_t>(it.r) * kPfRows + row < L;   // rows past L are written as zeros
       const int64_t grow = static_cast<int64_t>(it.b) * a.lpad + static_cast<int64_t>(it.r) * kPfRows + row;
-      if (it.g == 0) {
+      if (it.g == 0 && it.live) {
         // the row's rope key, copied beside K_nope so that the attention kernel reads whole
         // 128-row tiles without page lookups (zeros past the sequence's length)
         uint4 rv[8];
@@ -285,30 +334,32 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         good = __all_sync(0xffffffffu, good);
         if (!good) { ok = false; break; }
         tc::tc_fence_after();
-        const int n0 = (it.g * kKvTilesPerItem + t) * kKvNt;
-        uint16_t* dst = (n0 < kH * kDh ? a.k_buf + n0 : a.v_buf + (n0 - kH * kDh)) + grow * (kH * kDh);
+        if (it.live) {
+          const int n0 = (it.g * kKvTilesPerItem + t) * kKvNt;
+          uint16_t* dst = (n0 < kH * kDh ? a.k_buf + n0 : a.v_buf + (n0 - kH * kDh)) + grow * (kH * kDh);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kKvNt; c0 += 32) {
-          uint32_t r[32];
-          tc::tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + 256 * buf + c0, r);
-          tc::tmem_ld_wait();
-          uint32_t w[16];
-          if (n0 < kH * kDh) {
+          for (int c0 = 0; c0 < kKvNt; c0 += 32) {
+            uint32_t r[32];
+            tc::tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + 256 * buf + c0, r);
+            tc::tmem_ld_wait();
+            uint32_t w[16];
+            if (n0 < kH * kDh) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-              w[u] = valid ? tc::pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])) : 0u;
-          } else {
+              for (int u = 0; u < 16; ++u)
+                w[u] = valid ? tc::pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])) : 0u;
+            } else {
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-              w[u] = valid ? pack_f16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])) : 0u;
+              for (int u = 0; u < 16; ++u)
+                w[u] = valid ? pack_f16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])) : 0u;
+            }
+            uint4* o = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) o[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           }
-          uint4* o = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) o[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&S->d_free[buf]);
+        if (lane == 0) tc::mbar_arrive_cluster(d_free0 + 8u * buf);
       }
     }
     if (!ok) kv_set_abort(S);
@@ -316,8 +367,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc::tc_fence_before();
   __syncthreads();
+  tc::cluster_sync();   // no pair MMA, remote arrive or TMEM access of the other CTA is left
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc<512>(tm);
+  if (warp == 1) tc::tmem_dealloc_pair<512>(tm);
 }
 
 // ------------------------------------------------------------------ prefill_attn_kernel
