@@ -612,11 +612,65 @@ def cpu_baseline(inp, seconds):
                       f"visited / n_heads / time; numpy's BLAS pool had {blas_threads()} threads"}
 
 
+def oracle_prefill_sample(inp, seconds: float, step: int = 0):
+    """Time the fp64 oracle's prefill (explicit form) on a bounded sample of one prefill step:
+    (sequence, head) pairs, all new tokens of each, until the budget is used. Returns prompt tokens
+    per second (query rows per second over all heads / n_heads), the pairs done and the time."""
+    from oracle import mla_oracle as O
+    s = inp.shape
+    pf = S.draw_prefill(inp, step=step)
+    rng = np.random.default_rng(step)
+    w_uk, w_uv = inp.w_uk.double().numpy(), inp.w_uv.double().numpy()
+    qn, qr = pf.q_nope.double().numpy(), pf.q_rope.double().numpy()
+    inv_freq = O.yarn_inv_freq(s.d_rope, s.rope_theta, s.yarn_factor, s.yarn_alpha, s.yarn_beta, s.yarn_orig_len)
+    b = int(rng.integers(0, s.batch))
+    o0, o1 = int(inp.token_offsets[b]), int(inp.token_offsets[b + 1])
+    c, kr, _ = O.append_rows(inp.c_kv_raw[o0:o1].double().numpy(), inp.k_rope_raw[o0:o1].double().numpy(),
+                             np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta,
+                             inv_freq=inv_freq)
+    n = int(pf.n_new[b])
+    rows = list(range(int(pf.q_start[b]), int(pf.q_start[b]) + n))
+    cs = [c if k == b else np.zeros((0, s.d_c)) for k in range(s.batch)]
+    ks = [kr if k == b else np.zeros((0, s.d_rope)) for k in range(s.batch)]
+    n_new = [n if k == b else 0 for k in range(s.batch)]
+    sl = slice(int(pf.q_start[b]), int(pf.q_start[b]) + n)
+    t0 = time.perf_counter()
+    done = 0
+    for i in rng.permutation(s.n_heads):
+        O.prefill(qn[sl], qr[sl], w_uk, w_uv, cs, ks, n_new, s.scale * O.yarn_logit_factor(s.yarn_factor, s.yarn_mscale),
+                  heads=[int(i)])
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return n * done / s.n_heads / dt, done, dt
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
     shape = S.SHAPES[args.workload]
     inp = S.make_inputs(shape)
+    if args.workload in S.PREFILL_SHAPES:
+        vals, secs = [], 0.0
+        per_step = max(0.5, args.cpu_seconds / max(1, args.steps))
+        for k in range(args.warmup):
+            oracle_prefill_sample(inp, min(1.0, args.cpu_seconds / 10), k)
+        for k in range(args.steps):
+            v, done, dt = oracle_prefill_sample(inp, per_step, args.warmup + k)
+            vals.append(v)
+            secs += dt
+        value = float(np.mean(vals))
+        return {"impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded; random-init weights)",
+                "config": {"workload": shape.name, "batch": shape.batch, "prompt_len": int(inp.lengths.max()),
+                           "n_heads": shape.n_heads, "cache_dtype": shape.cache_dtype, "parallelism": "host cores"},
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                                 "sample": f"each step: {per_step:.1f} s of single-head fp64 explicit-form prefills "
+                                           f"of one {shape.name} prompt; numpy's BLAS pool had {blas_threads()} threads"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     for k in range(args.warmup):
         oracle_sample(inp, min(1.0, args.cpu_seconds / 10), k)
     vals, secs = [], 0.0
@@ -651,8 +705,14 @@ def main():
         res, inp = run_prefill(args, rank, world, local)
     else:
         res, inp = run_gpu(args, rank, world, local)
-    if rank == 0:
-        if not args.no_cpu_baseline and args.workload not in S.PREFILL_SHAPES:
+    if rank == 0 and not args.no_cpu_baseline:
+        if args.workload in S.PREFILL_SHAPES:
+            v, done, dt = oracle_prefill_sample(inp, args.cpu_seconds)
+            res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                                   "sample": f"{done} single-head fp64 explicit-form prefills of one {inp.shape.name} "
+                                             f"prompt ({dt:.1f} s); tokens/s = prompt tokens x heads done / n_heads "
+                                             f"/ time; numpy's BLAS pool had {blas_threads()} threads"}
+        else:
             res["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
         print(json.dumps(res), flush=True)
     if world > 1:
