@@ -714,6 +714,7 @@ def main():
                                              f"/ time; numpy's BLAS pool had {blas_threads()} threads"}
         else:
             res["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+    if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
