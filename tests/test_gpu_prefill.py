@@ -35,12 +35,13 @@ def _oracle_prefill(inp, pf, heads=None, rows=None):
                      inp.w_uv.double().numpy(), cs, ks, pf.n_new, T.oracle_scale(inp.shape), heads=heads, rows=rows)
 
 
-@pytest.mark.parametrize("lengths,n_new", [
-    ((1, 130, 300), None),              # whole prompts: one row, a ragged tile tail, three tiles
-    ((200, 333, 64), (77, 333, 0)),     # a chunk after a 123-row prefix, a whole prompt, no new token
+@pytest.mark.parametrize("lengths,n_new,yarn", [
+    ((1, 130, 300), None, 1.0),              # whole prompts: one row, a ragged tile tail, three tiles
+    ((200, 333, 64), (77, 333, 0), 1.0),     # a chunk after a 123-row prefix, a whole prompt, no new token
+    ((260, 513), (260, 129), 40.0),          # the report's YaRN setting: scaled rope keys, logit factor
 ])
-def test_prefill_all_outputs_small(lengths, n_new):
-    shape = S.shape_with("prefill_b4", batch=len(lengths), lengths=lengths)
+def test_prefill_all_outputs_small(lengths, n_new, yarn):
+    shape = S.shape_with("prefill_b4", batch=len(lengths), lengths=lengths, yarn_factor=yarn)
     inp = S.make_inputs(shape)
     pf = S.draw_prefill(inp, None if n_new is None else np.array(n_new))
     out, M = _device_prefill(inp, pf)
