@@ -296,6 +296,25 @@ def run_gpu(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = job_value(world, tokens, args.steps, total_ms / 1e3)
 
+    # the decode alone (no append in the step), same timing rules
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        qn, qr, _, _ = dsteps[(args.warmup + k) % len(dsteps)]
+        flush_l2()
+        torch.cuda._sleep(2_000_000)
+        dev_ev[k][0].record(stream)
+        if hid:
+            M.decode_hidden(cfg, qn, qr, w_uk, w_ouv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        elif q == 1:
+            M.decode(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        else:
+            M.decode_multi(cfg, qn, qr, w_uk, w_uv, pool, bt, seq_lens, max_len, out=out, workspace=ws)
+        dev_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    dec_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in dev_ev), world, dev) / args.steps
+    decode_only = {"ms_per_step": round(dec_ms, 5), "value": job_value(world, tokens, 1, dec_ms / 1e3),
+                   "unit": UNIT}
+
     # per-kernel durations (separate pass, same steps, events between the kernels). A GPU-side
     # sleep ahead of each step lets the host enqueue all of the step's launches and events before
     # the first event fires, so an interval holds its kernel's GPU time and no host enqueue gap.
@@ -409,7 +428,8 @@ def run_gpu(args, rank, world, local):
                       "output": f"hidden {hid} (W_UV folded into W_O)" if hid else "per-head [B, H, d_head]",
                       "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB memset + 512 MiB read)",
                       "decode_path": "tcgen05" if M.decode_path(cfg) else "cuda-core"},
-           "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+           "roofline": roofline, "e2e": e2e, "decode_only": decode_only,
+           "gpu_launches": launches_per_step * args.steps,
            "pages_context": {"kv_cache_reduction_vs_67b": "93.3%",
                              "max_generation_throughput_vs_67b": "5.76x (end-to-end serving, 8x H800 node)",
                              "note": "the pages give no number for the decode kernel itself"},
