@@ -48,7 +48,6 @@ constexpr int kPrSoftmaxWarps = 8;
 constexpr uint32_t kPrTmS = 0;                      // score buffers at 0 and 128
 constexpr uint32_t kPrTmO = 256;                    // O: PV MMA 0 at 256, MMA 1 at 384
 constexpr int kPrKSteps = 18;                       // contraction steps of 16 per half (256 latent + 32 rope)
-constexpr int kPrEarlyBatch = 1024;                 // largest batch whose first tiles load before the plan is read
 constexpr int kPrF8Ahead = 8;                       // FP8 cache: tiles prefetched to L2 ahead of their loads
 
 struct PairSmem {
@@ -164,13 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
   tc::tc_fence_after();
   const uint32_t tm = S->tmem_base;
 
-  // The first tiles of this cluster's share go out before the wait on the absorb kernel: the
-  // producer warp derives the share from seq_lens exactly as the plan does (lengths clamped to
-  // [0, max_seq_len], ceil(L / 64) tiles, share [c T / n, (c + 1) T / n)) and requests up to one
-  // ring's worth of tiles. The cache, page table and lengths are complete before the absorb kernel
-  // starts (the decode's contract), so only the queries and the plan wait for it.
   uint32_t n_pre = 0;
-  int64_t pre_T = 0, pre_t0 = 0;
   const uint64_t policy = tc::policy_evict_first();
   auto issue_tile = [&](uint32_t it, int32_t y) {   // lane 0 of the producer warp; slots free for it < ring
     const int st = it % kPrStages;
@@ -193,59 +186,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
   };
   // pool row of tile j of sequence b (or a row outside the pool, which loads zeros, for a bad page id)
   auto tile_row = [&](int b, int j) -> int32_t {
-    const int64_t tok = static_cast<int64_t>(j) * kTile;
-    const int pg = static_cast<int>(tok / a.page_size);
-    int64_t page = -1;
-    if (pg < a.max_pages)
-      page = a.block_table ? a.block_table[static_cast<int64_t>(b) * a.max_pages + pg]
-                           : static_cast<int64_t>(b) * a.max_pages + pg;
-    if (page < 0 || page >= a.num_pages) {
-      flag_error(ERR_BIT_BOUNDS);
-      return -2 * kTile;
-    }
-    return static_cast<int32_t>(page * a.page_size + tok % a.page_size);
+    return cache_tile_row(a.block_table, b, j, a.max_pages, a.page_size, a.num_pages);
   };
-  if (warp == 0 && a.batch <= kPrEarlyBatch) {
-    auto tiles_of = [&](int bb) -> int {
-      if (bb >= a.batch) return 0;
-      int L = a.seq_lens[bb];
-      L = L < 0 ? 0 : (L > a.max_seq_len ? a.max_seq_len : L);
-      return (L + kTile - 1) / kTile;
-    };
-    for (int base = 0; base < a.batch; base += 32) {
-      int n = tiles_of(base + lane);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-      pre_T += n;
-    }
-    pre_t0 = share_begin(cl, pre_T, ncl);
-    const int64_t t1 = share_begin(cl + 1, pre_T, ncl);
-    const int ring = kF8 ? CF::kRaw : kPrStages;
-    const int want = static_cast<int>(min(static_cast<int64_t>(ring), t1 - pre_t0));
-    // walk the sequences to tile pre_t0 and request the next `want` tiles
-    int64_t acc = 0;
-    int b = 0;
-    while (want > 0 && b < a.batch) {
-      const int n = tiles_of(b);
-      if (acc + n > pre_t0) break;
-      acc += n;
-      ++b;
-    }
-    int j = static_cast<int>(pre_t0 - acc);
-    for (int k = 0; k < want && b < a.batch; ++k) {
-      while (b < a.batch && j >= tiles_of(b)) { j = 0; ++b; }
-      if (b >= a.batch) break;
-      const int32_t y = tile_row(b, j);
-      if (lane == 0) issue_tile(n_pre, y);
-      ++n_pre;
-      ++j;
-    }
-  }
 
   // everything below reads what the absorb kernel wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t* cum = a.plan.cum;
-  const uint32_t n_share = static_cast<uint32_t>(a.plan.share_start[cl + 1] - a.plan.share_start[cl]);
+  const uint32_t n_share = static_cast<uint32_t>(a.plan.share_tiles[cl]);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- cache tiles (both CTAs: own half)
@@ -253,10 +200,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
     int b, j0, j1;
     uint32_t it = 0;
     bool ok = true;
-    if (n_pre > 0 && (pre_T != cum[a.batch] || pre_t0 != a.plan.share_start[cl])) {
-      // the lengths changed after this kernel read them: the decode's contract was broken
-      flag_error(ERR_BIT_BOUNDS);
-      ok = false;
+    {
+      // the share's first tiles, whose pool rows the plan holds, go out at once
+      constexpr uint32_t ring = kF8 ? CF::kRaw : kPrStages;
+      static_assert(ring <= kPlanRows, "the plan holds the rows of one ring of tiles");
+      n_pre = min(ring, n_share);
+      int32_t y = 0;
+      if (lane < n_pre) y = a.plan.first_rows[cl * kPlanRows + lane];
+      for (uint32_t k = 0; k < n_pre; ++k) {
+        const int32_t yk = __shfl_sync(0xffffffffu, y, k);
+        if (lane == 0) issue_tile(k, yk);
+      }
     }
     while (ok && si.next(cum, a.batch, &b, &j0, &j1)) {
       for (int jc = j0; jc < j1 && ok; jc += 32) {
@@ -276,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
           const int32_t y = __shfl_sync(0xffffffffu, y_l, u);
           const int32_t y_ahead = __shfl_sync(0xffffffffu, y_l, (u + kPrF8Ahead) & 31);
           if (kF8 && lane == 0 && u + kPrF8Ahead < n) l2_tile(y_ahead);
-          if (lane == 0 && ok && it >= n_pre) {   // tiles before n_pre went out before the wait
+          if (lane == 0 && ok && it >= n_pre) {   // tiles before n_pre went out from the plan's rows
             const int st = it % kPrStages;
             if (it >= kPrStages) ok = tc::mbar_wait(&S->empty[st], ((it / kPrStages) - 1) & 1);
             if (kF8 && ok && it >= 2) ok = tc::mbar_wait(&S->raw_empty[it & 1], ((it / 2) - 1) & 1);
@@ -290,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kF8>::kThrea
       }
     }
     it = __shfl_sync(0xffffffffu, it, 0);
-    if (it < n_pre) it = n_pre;   // tiles requested before the wait are in flight too
+    if (it < n_pre) it = n_pre;   // the tiles requested from the plan's rows are in flight too
     if (lane == 0) {
       if (!ok) pr_set_abort(S);
       // copies still in flight must land before the CTA exits

@@ -42,19 +42,30 @@ __host__ __device__ __forceinline__ int64_t parto_index(int64_t slot, int chunk,
   return ((slot * kOChunks + chunk) * kH + head) * 4;
 }
 
+// The clusters split the work in units: a sequence with tiles counts its tiles plus kSegUnits for
+// the start of a segment (its queries' load, the pipeline fill and the partial's write, about three
+// tiles' time), so a cluster whose share crosses into another sequence gets fewer tiles. Tile j of
+// sequence b is unit cum[b] + kSegUnits + j.
+constexpr int kSegUnits = 3;
+// Pool rows of the first kPlanRows tiles of each share are in the plan, so that the attend kernel
+// requests them as soon as the plan is ready, without walking the plan and the page table first.
+constexpr int kPlanRows = 4;
+
 struct Plan {
   int32_t* lens;         // [B] lengths clamped to [0, max_seq_len]
-  int32_t* cum;          // [B+1] prefix sums of ceil(len / 64)
-  int32_t* first_seq;    // [clusters] sequence holding the first tile of each cluster's share
-  int32_t* share_start;  // [clusters + 1] first tile of each cluster's share (share c = [start[c], start[c+1]))
-  int32_t* seq_c0;       // [B] first cluster whose share meets sequence b's tiles (when it has any)
+  int32_t* cum;          // [B+1] prefix sums of units(b) = tiles(b) + kSegUnits (0 for a sequence without tiles)
+  int32_t* first_seq;    // [clusters] sequence holding the first unit of each cluster's share
+  int32_t* share_start;  // [clusters + 1] first unit of each cluster's share (share c = [start[c], start[c+1]))
+  int32_t* seq_c0;       // [B] first cluster whose share holds tiles of sequence b (when it has any)
   int32_t* seq_c1;       // [B] last such cluster
+  int32_t* share_tiles;  // [clusters] tiles in each cluster's share
+  int32_t* first_rows;   // [clusters][kPlanRows] pool rows of each share's first tiles (see cache_tile_row)
 };
 
-// Tile range [t0, t1) of cluster c when T tiles are split over nc clusters.
+// Unit range [t0, t1) of cluster c when T units are split over nc clusters.
 __host__ __device__ __forceinline__ int64_t share_begin(int64_t c, int64_t T, int64_t nc) { return c * T / nc; }
 
-// The cluster whose share holds tile t (T > 0).
+// The cluster whose share holds unit t (T > 0).
 __host__ __device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, int64_t nc) {
   return ((t + 1) * nc - 1) / T;
 }
@@ -63,14 +74,77 @@ __host__ __device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, in
 struct AbsorbArgs {
   const uint16_t* q_rope;     // [B, H, 64]
   const int32_t* seq_lens;    // [B]
+  const int32_t* block_table; // [B, max_pages] (NULL: contiguous, sequence b owns pages b*max_pages ..)
   uint16_t* q_lat;            // row-major [B, H, 576], see qlat_row_index
   Plan plan;
+  int64_t num_pages;
+  int max_pages, page_size;
   int batch, nb, max_seq_len, ncl;
   int f16_lat;                // 1: the latent part of Q_lat in fp16 (the operand type of an FP8 cache's tiles)
 };
 
 __host__ __device__ __forceinline__ int64_t qlat_row_index(int64_t b, int head, int k) {
   return (b * kH + head) * kRow + k;
+}
+
+struct SegIter {
+  int64_t t, t1;  // next unit (global index) and end of share
+  int b;          // current sequence
+  // the next (sequence, tile range [j0, j1)) with at least one tile; false at the share's end
+  __host__ __device__ __forceinline__ bool next(const int32_t* cum, int batch, int* seq, int* j0, int* j1) {
+    while (t < t1) {
+      while (b < batch && cum[b + 1] <= t) ++b;
+      if (b >= batch) return false;
+      const int64_t first = cum[b] + kSegUnits;   // unit of the sequence's tile 0
+      const int64_t start = t > first ? t : first;
+      const int64_t end = t1 < cum[b + 1] ? t1 : static_cast<int64_t>(cum[b + 1]);
+      t = end;
+      if (start < end) {
+        *seq = b;
+        *j0 = static_cast<int>(start - first);
+        *j1 = static_cast<int>(end - first);
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+// Tiles in the unit range [t0, t1) whose first unit lies in sequence `first` (units less the
+// segment-start units the range holds); with fb / fj, also the sequence and tile index of the
+// range's first kPlanRows tiles (entries past the count are left alone).
+__host__ __device__ __forceinline__ int64_t share_tile_count(const int32_t* cum, int batch, int first, int64_t t0,
+                                                             int64_t t1, int* fb = nullptr, int* fj = nullptr) {
+  SegIter si{t0, t1, first};
+  int b, j0, j1;
+  int64_t n = 0;
+  while (si.next(cum, batch, &b, &j0, &j1)) {
+    if (fb)
+      for (int64_t k = n; k < kPlanRows && k < n + (j1 - j0); ++k) {
+        fb[k] = b;
+        fj[k] = j0 + static_cast<int>(k - n);
+      }
+    n += j1 - j0;
+  }
+  return n;
+}
+
+// Pool row of tile j (tokens 64 j ..) of sequence b: page block_table[b][64 j / page_size] (or
+// b * max_pages + that index without a table), row 64 j mod page_size within it. A page id outside
+// [0, num_pages) or a page index past max_pages flags a bounds error and gives a row outside the
+// pool, which a tile load fills with zeros.
+__device__ __forceinline__ int32_t cache_tile_row(const int32_t* block_table, int b, int j, int max_pages,
+                                                  int page_size, int64_t num_pages) {
+  const int64_t tok = static_cast<int64_t>(j) * kTile;
+  const int pg = static_cast<int>(tok / page_size);
+  int64_t page = -1;
+  if (pg < max_pages)
+    page = block_table ? block_table[static_cast<int64_t>(b) * max_pages + pg] : static_cast<int64_t>(b) * max_pages + pg;
+  if (page < 0 || page >= num_pages) {
+    flag_error(ERR_BIT_BOUNDS);
+    return -2 * kTile;
+  }
+  return static_cast<int32_t>(page * page_size + tok % page_size);
 }
 
 constexpr int kAbsorbThreads = 128;
@@ -95,6 +169,7 @@ __device__ void plan_block(const AbsorbArgs& a) {
       }
       a.plan.lens[b] = L;
       n = (L + kTile - 1) / kTile;
+      if (n > 0) n += kSegUnits;
     }
     int x = n;  // inclusive warp scan
 #pragma unroll
@@ -123,11 +198,20 @@ __device__ void plan_block(const AbsorbArgs& a) {
       if (a.plan.cum[mid] <= t) lo = mid; else hi = mid;
     }
     a.plan.first_seq[c] = lo;
+    int fb[kPlanRows], fj[kPlanRows];
+    const int64_t n = share_tile_count(a.plan.cum, a.batch, lo, t, share_begin(c + 1, T, a.ncl), fb, fj);
+    a.plan.share_tiles[c] = static_cast<int32_t>(n);
+    int32_t rows[kPlanRows];
+#pragma unroll
+    for (int k = 0; k < kPlanRows; ++k)   // independent page-table loads
+      rows[k] = k < n ? cache_tile_row(a.block_table, fb[k], fj[k], a.max_pages, a.page_size, a.num_pages) : 0;
+#pragma unroll
+    for (int k = 0; k < kPlanRows; ++k) a.plan.first_rows[c * kPlanRows + k] = rows[k];
   }
   for (int b = threadIdx.x; b < a.batch; b += kAbsorbThreads) {
     const int64_t tb0 = a.plan.cum[b], tb1 = a.plan.cum[b + 1];
     if (tb1 > tb0) {
-      a.plan.seq_c0[b] = static_cast<int32_t>(share_owner(tb0, T, a.ncl));
+      a.plan.seq_c0[b] = static_cast<int32_t>(share_owner(tb0 + kSegUnits, T, a.ncl));   // its first tile
       a.plan.seq_c1[b] = static_cast<int32_t>(share_owner(tb1 - 1, T, a.ncl));
     } else {
       a.plan.seq_c0[b] = 0;
@@ -238,7 +322,6 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
 struct AttendArgs {
   const uint16_t* q_lat;      // row-major [B, H, 576], see qlat_row_index
   const int32_t* block_table; // [B, max_pages] (NULL: contiguous, sequence b owns pages b*max_pages ..)
-  const int32_t* seq_lens;    // [B] as given to the decode (read before the plan exists)
   int max_seq_len;
   Plan plan;
   float* part_o;              // chunk-major (see parto_index) fp32, unnormalised
@@ -249,21 +332,6 @@ struct AttendArgs {
 };
 
 // Segment iterator: the (sequence, tile range) pieces of this cluster's share.
-struct SegIter {
-  int64_t t, t1;  // next tile (global index) and end of share
-  int b;          // current sequence
-  __device__ __forceinline__ bool next(const int32_t* cum, int batch, int* seq, int* j0, int* j1) {
-    if (t >= t1) return false;
-    while (b < batch && cum[b + 1] <= t) ++b;
-    if (b >= batch) return false;
-    const int64_t end = min(t1, static_cast<int64_t>(cum[b + 1]));
-    *seq = b;
-    *j0 = static_cast<int>(t - cum[b]);
-    *j1 = static_cast<int>(end - cum[b]);
-    t = end;
-    return true;
-  }
-};
 
 __device__ __forceinline__ SegIter seg_begin(const Plan& plan, int batch, uint32_t c, uint32_t nc) {
   (void)batch;

@@ -236,7 +236,8 @@ constexpr int kMaxClusters = 128;
 
 struct TcPlan {
   int nb, slots;
-  size_t off_qlat, off_lens, off_cum, off_first, off_start, off_c0, off_c1, off_ml, off_o, off_hi, off_lo, bytes;
+  size_t off_qlat, off_lens, off_cum, off_first, off_start, off_c0, off_c1, off_tiles, off_rows, off_ml, off_o, off_hi,
+      off_lo, bytes;
 };
 
 TcPlan tc_plan(int batch) {
@@ -258,6 +259,10 @@ TcPlan tc_plan(int batch) {
   off = align_up(off + static_cast<size_t>(batch) * 4, 256);
   p.off_c1 = off;
   off = align_up(off + static_cast<size_t>(batch) * 4, 256);
+  p.off_tiles = off;
+  off = align_up(off + static_cast<size_t>(kMaxClusters) * 4, 256);
+  p.off_rows = off;
+  off = align_up(off + static_cast<size_t>(kMaxClusters) * tcd::kPlanRows * 4, 256);
   p.off_ml = off;
   off = align_up(off + static_cast<size_t>(p.slots) * tcd::kH * 8, 256);
   p.off_o = off;
@@ -378,7 +383,8 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   tcd::Plan plan{reinterpret_cast<int32_t*>(ws + p.off_lens), reinterpret_cast<int32_t*>(ws + p.off_cum),
                  reinterpret_cast<int32_t*>(ws + p.off_first), reinterpret_cast<int32_t*>(ws + p.off_start),
-                 reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1)};
+                 reinterpret_cast<int32_t*>(ws + p.off_c0), reinterpret_cast<int32_t*>(ws + p.off_c1),
+                 reinterpret_cast<int32_t*>(ws + p.off_tiles), reinterpret_cast<int32_t*>(ws + p.off_rows)};
   uint16_t* q_lat = reinterpret_cast<uint16_t*>(ws + p.off_qlat);
 
   CUtensorMap m_lat, m_scale, m_rope, m_wuk, m_wuv, m_qn, m_hi, m_lo, m_q, m_qr;
@@ -437,6 +443,10 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   tcd::AbsorbArgs aa{};
   aa.q_rope = static_cast<const uint16_t*>(q_rope);
   aa.seq_lens = seq_lens;
+  aa.block_table = block_table;
+  aa.num_pages = num_pages;
+  aa.max_pages = max_pages;
+  aa.page_size = c->page_size;
   aa.q_lat = q_lat;
   aa.plan = plan;
   aa.batch = batch;
@@ -448,7 +458,6 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   tcd::AttendArgs ta{};
   ta.q_lat = q_lat;
   ta.block_table = block_table;
-  ta.seq_lens = seq_lens;
   ta.max_seq_len = max_seq_len;
   ta.plan = plan;
   ta.part_o = reinterpret_cast<float*>(ws + p.off_o);
