@@ -167,12 +167,8 @@ MLA_API size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, i
  *   - the first one may start reading W_UK before the kernel that precedes
  *     mla_decode on `stream` has finished, so that kernel must not write the
  *     weights;
- *   - the attend kernel reads seq_lens, block_table and the pool as soon as
- *     the first one has started, so the preceding kernel must have finished
- *     writing them before it allows dependent launches. An ordinary kernel
- *     (one that never executes griddepcontrol.launch_dependents) allows them
- *     only when it exits, and always satisfies this.
- * q_nope and q_rope are read only after the preceding kernel completes.
+ *   - every other input (q_nope, q_rope, seq_lens, block_table, the pool) is
+ *     read only after the preceding kernel completes.
  */
 MLA_API mla_status mla_decode(const mla_config* cfg, const void* q_nope, const void* q_rope,
                       const void* w_uk, const void* w_uv, const void* pool, int64_t num_pages,
