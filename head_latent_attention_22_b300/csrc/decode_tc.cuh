@@ -149,12 +149,18 @@ __device__ __forceinline__ int32_t cache_tile_row(const int32_t* block_table, in
 
 constexpr int kAbsorbThreads = 128;
 
-__device__ void plan_block(const AbsorbArgs& a) {
+// Prefix sums the plan block keeps in shared memory (the absorb kernel's dynamic shared memory,
+// unused by this block): the share searches read them there for batches below this size.
+constexpr int kPlanSmemRows = 16384;
+
+__device__ void plan_block(const AbsorbArgs& a, int32_t* cum_s) {
+  const bool in_smem = a.batch < kPlanSmemRows;
   __shared__ int32_t carry;
   __shared__ int32_t warp_tot[kAbsorbThreads / 32];
   if (threadIdx.x == 0) {
     carry = 0;
     a.plan.cum[0] = 0;
+    cum_s[0] = 0;
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -181,13 +187,17 @@ __device__ void plan_block(const AbsorbArgs& a) {
     __syncthreads();
     int off = carry;
     for (int w = 0; w < warp; ++w) off += warp_tot[w];
-    if (b < a.batch) a.plan.cum[b + 1] = off + x;
+    if (b < a.batch) {
+      a.plan.cum[b + 1] = off + x;
+      if (in_smem) cum_s[b + 1] = off + x;
+    }
     __syncthreads();
     if (threadIdx.x == kAbsorbThreads - 1) carry = off + x;
     __syncthreads();
   }
   // cluster shares: start tile and first sequence of each; clusters of each sequence
-  const int64_t T = a.plan.cum[a.batch];
+  const int32_t* cum = in_smem ? cum_s : a.plan.cum;
+  const int64_t T = cum[a.batch];
   for (int c = threadIdx.x; c <= a.ncl; c += kAbsorbThreads) {
     const int64_t t = share_begin(c, T, a.ncl);
     a.plan.share_start[c] = static_cast<int32_t>(t);
@@ -195,11 +205,11 @@ __device__ void plan_block(const AbsorbArgs& a) {
     int lo = 0, hi = a.batch;   // cum[lo] <= t
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (a.plan.cum[mid] <= t) lo = mid; else hi = mid;
+      if (cum[mid] <= t) lo = mid; else hi = mid;
     }
     a.plan.first_seq[c] = lo;
     int fb[kPlanRows], fj[kPlanRows];
-    const int64_t n = share_tile_count(a.plan.cum, a.batch, lo, t, share_begin(c + 1, T, a.ncl), fb, fj);
+    const int64_t n = share_tile_count(cum, a.batch, lo, t, share_begin(c + 1, T, a.ncl), fb, fj);
     a.plan.share_tiles[c] = static_cast<int32_t>(n);
     int32_t rows[kPlanRows];
 #pragma unroll
@@ -209,7 +219,7 @@ __device__ void plan_block(const AbsorbArgs& a) {
     for (int k = 0; k < kPlanRows; ++k) a.plan.first_rows[c * kPlanRows + k] = rows[k];
   }
   for (int b = threadIdx.x; b < a.batch; b += kAbsorbThreads) {
-    const int64_t tb0 = a.plan.cum[b], tb1 = a.plan.cum[b + 1];
+    const int64_t tb0 = cum[b], tb1 = cum[b + 1];
     if (tb1 > tb0) {
       a.plan.seq_c0[b] = static_cast<int32_t>(share_owner(tb0 + kSegUnits, T, a.ncl));   // its first tile
       a.plan.seq_c1[b] = static_cast<int32_t>(share_owner(tb1 - 1, T, a.ncl));
@@ -229,12 +239,23 @@ __global__ void __launch_bounds__(kAbsorbThreads) absorb_tc_kernel(const __grid_
                                                                    const __grid_constant__ CUtensorMap map_qn,
                                                                    AbsorbArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint8_t smem_raw[];
   if (blockIdx.x == 2 * kH) {
+    // the lengths and the page table go to L2 while the kernel ahead finishes (a prefetch reads
+    // nothing, so a kernel that still writes them is no hazard: L2 holds the one copy)
+    const char* pl = reinterpret_cast<const char*>(a.seq_lens);
+    for (int64_t o = 128 * threadIdx.x; o < 4 * static_cast<int64_t>(a.batch); o += 128 * kAbsorbThreads)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(pl + o));
+    if (a.block_table) {
+      const char* pt = reinterpret_cast<const char*>(a.block_table);
+      const int64_t nbytes = min(4 * static_cast<int64_t>(a.batch) * a.max_pages, static_cast<int64_t>(1) << 19);
+      for (int64_t o = 128 * threadIdx.x; o < nbytes; o += 128 * kAbsorbThreads)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(pt + o));
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    plan_block(a);
+    plan_block(a, reinterpret_cast<int32_t*>(smem_raw));
     return;
   }
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = sm;                          // 4 boxes [128 d_h rows x 64 latent] = 64 KB
   uint8_t* sB = sm + 4 * 16384;              // 2 boxes [nb rows x 64 d_h]
@@ -374,81 +395,103 @@ struct MergeArgs {
   int f16;               // 1: fp16 pair (the operand type of the folded output GEMM)
 };
 
-constexpr int kMergeSplit = kOChunks;            // CTAs per sequence: one 4-float chunk each
-
-// One CTA per (sequence b, 4 latent elements); thread = head. o_lat =
-// sum_s w_s O_s / sum_s w_s l_s with w_s = 2^(m_s - max m) over the partials
-// of b's segments (slots b + c for the clusters c whose shares meet b's
-// tiles). Every load is a warp reading 32 consecutive heads of one chunk.
+// One CTA per (sequence b, kG chunks of 4 latent elements); thread = head.
+// o_lat = sum_s w_s O_s / sum_s w_s l_s with w_s = 2^(m_s - max m) over the
+// partials of b's segments (slots b + c for the clusters c whose shares meet
+// b's tiles), as an online log-sum-exp over kS slots at a time: the (m, l)
+// pairs and the kG chunks of kS slots are loaded together, one round trip per
+// group. Small batches take one chunk per CTA (enough CTAs to fill the GPU);
+// larger ones four, so that fewer, longer CTAs do the work. Every load is a
+// warp reading 32 consecutive heads of one chunk.
+template <int kG, int kS>
 __global__ void __launch_bounds__(kH) merge_kernel(MergeArgs a) {
+  static_assert(kG == 1 || kG % 2 == 0, "chunks are stored 8 or 16 elements at a time");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int h = threadIdx.x;
   const int b = blockIdx.y;
-  const int chunk = blockIdx.x;
+  const int ch0 = blockIdx.x * kG;
   const int c0 = a.plan.seq_c0[b], c1 = a.plan.seq_c1[b];   // c1 < c0: no tiles, output 0
   const int32_t* start = a.plan.share_start;
   const float2* ml_all = reinterpret_cast<const float2*>(a.part_ml);
-  // online log-sum-exp over the partials, eight at a time so their loads overlap
   float M = -INFINITY, den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int cb = c0; cb <= c1; cb += 8) {
-    float4 o[8];
-    float2 ml[8];
-    bool use[8];
+  float4 acc[kG];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+  for (int k = 0; k < kG; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cb = c0; cb <= c1; cb += kS) {
+    float4 o[kS][kG];
+    float2 ml[kS];
+    bool use[kS];
+#pragma unroll
+    for (int u = 0; u < kS; ++u) {
       // the loads do not wait for the share check: a slot of an empty share (which wrote
       // no partial) is read and then ignored, so all loads are one round trip
       const int c = cb + u;
       use[u] = c <= c1 && start[c] < start[c + 1];
       if (c <= c1) {
         ml[u] = ml_all[static_cast<int64_t>(b + c) * kH + h];
-        o[u] = *reinterpret_cast<const float4*>(a.part_o + parto_index(b + c, chunk, h));
+#pragma unroll
+        for (int k = 0; k < kG; ++k)
+          o[u][k] = *reinterpret_cast<const float4*>(a.part_o + parto_index(b + c, ch0 + k, h));
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kS; ++u) {
       if (!use[u]) continue;
       float w = 1.f;
       if (ml[u].x > M) {
         const float r = exp2f(M - ml[u].x);   // 0 on the first partial (M = -inf)
-        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+        for (int k = 0; k < kG; ++k) {
+          acc[k].x *= r; acc[k].y *= r; acc[k].z *= r; acc[k].w *= r;
+        }
         den *= r;
         M = ml[u].x;
       } else {
         w = exp2f(ml[u].x - M);
       }
-      acc.x = fmaf(w, o[u].x, acc.x);
-      acc.y = fmaf(w, o[u].y, acc.y);
-      acc.z = fmaf(w, o[u].z, acc.z);
-      acc.w = fmaf(w, o[u].w, acc.w);
+#pragma unroll
+      for (int k = 0; k < kG; ++k) {
+        acc[k].x = fmaf(w, o[u][k].x, acc[k].x);
+        acc[k].y = fmaf(w, o[u][k].y, acc[k].y);
+        acc[k].z = fmaf(w, o[u][k].z, acc[k].z);
+        acc[k].w = fmaf(w, o[u][k].w, acc[k].w);
+      }
       den = fmaf(w, ml[u].y, den);
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  const float v[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
-  uint32_t hi[2], lo[2];
-  if (a.f16) {
+  uint32_t hi[2 * kG], lo[2 * kG];
+#pragma unroll
+  for (int k = 0; k < kG; ++k) {
+    const float v[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv};
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const __half h0 = __float2half_rn(v[2 * u]), h1 = __float2half_rn(v[2 * u + 1]);
-      const __half l0 = __float2half_rn(v[2 * u] - __half2float(h0));
-      const __half l1 = __float2half_rn(v[2 * u + 1] - __half2float(h1));
-      hi[u] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-      lo[u] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
-    }
-  } else {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      hi[u] = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
-      lo[u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(hi[u] & 0xffffu)),
-                            v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(hi[u] >> 16)));
+      if (a.f16) {
+        const __half h0 = __float2half_rn(v[2 * u]), h1 = __float2half_rn(v[2 * u + 1]);
+        const __half l0 = __float2half_rn(v[2 * u] - __half2float(h0));
+        const __half l1 = __float2half_rn(v[2 * u + 1] - __half2float(h1));
+        hi[2 * k + u] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+        lo[2 * k + u] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+      } else {
+        const uint32_t p = tc::pack_bf16(v[2 * u], v[2 * u + 1]);
+        hi[2 * k + u] = p;
+        lo[2 * k + u] = tc::pack_bf16(v[2 * u] - bf16_to_f32(static_cast<uint16_t>(p & 0xffffu)),
+                                      v[2 * u + 1] - bf16_to_f32(static_cast<uint16_t>(p >> 16)));
+      }
     }
   }
-  const int64_t e = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * chunk;
-  *reinterpret_cast<uint2*>(a.o_hi + e) = make_uint2(hi[0], hi[1]);
-  *reinterpret_cast<uint2*>(a.o_lo + e) = make_uint2(lo[0], lo[1]);
+  const int64_t e = (static_cast<int64_t>(b) * kH + h) * kDc + 4 * ch0;   // 4 kG elements, 8 kG-byte aligned
+  if constexpr (kG == 1) {
+    *reinterpret_cast<uint2*>(a.o_hi + e) = make_uint2(hi[0], hi[1]);
+    *reinterpret_cast<uint2*>(a.o_lo + e) = make_uint2(lo[0], lo[1]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < kG / 2; ++q) {
+      reinterpret_cast<uint4*>(a.o_hi + e)[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+      reinterpret_cast<uint4*>(a.o_lo + e)[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+    }
+  }
 }
 
 // ================================================================== W_UV

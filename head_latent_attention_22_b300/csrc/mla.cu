@@ -279,6 +279,8 @@ static_assert(tcd::PairCfg<false>::kSmem <= 232448, "attend kernel shared memory
 static_assert(tcd::PairCfg<true>::kSmem <= 232448, "attend kernel (FP8 cache) shared memory exceeds 227 KB");
 constexpr size_t kUvSmem = 1024 + tcd::kUvSmem;
 size_t absorb_smem(int nb) { return 1024 + 4 * 16384 + 2 * static_cast<size_t>(nb) * 128 + 64; }
+static_assert(4 * static_cast<size_t>(tcd::kPlanSmemRows) <= 1024 + 4 * 16384,
+              "the plan block's prefix sums fit the absorb kernel's shared memory");
 
 struct TcDeviceState {
   bool ready = false;
@@ -498,8 +500,13 @@ mla_status decode_tc(const mla_config* c, const void* q_nope, const void* q_rope
   if (s != MLA_OK) return s;
   stage_mark(2, st);
   void* merge_args[] = {&ma};
-  s = launch_pdl(reinterpret_cast<const void*>(tcd::merge_kernel), dim3(tcd::kMergeSplit, batch), dim3(tcd::kH), 0,
-                 st, merge_args);
+  // four chunks per CTA once that still gives two CTAs per SM (2 ncl SMs), else one
+  if (static_cast<int64_t>(batch) * (tcd::kOChunks / 4) >= 4 * static_cast<int64_t>(ncl))
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::merge_kernel<4, 8>), dim3(tcd::kOChunks / 4, batch),
+                   dim3(tcd::kH), 0, st, merge_args);
+  else
+    s = launch_pdl(reinterpret_cast<const void*>(tcd::merge_kernel<1, 16>), dim3(tcd::kOChunks, batch), dim3(tcd::kH),
+                   0, st, merge_args);
   if (s != MLA_OK) return s;
   stage_mark(3, st);
   if (w_ouv) {
