@@ -161,7 +161,7 @@ MLA_API size_t mla_decode_workspace_size(const mla_config* cfg, int32_t batch, i
  * Kernels: n_heads 128, d_c 512, d_rope 64, d_head 128 with bf16 queries and
  * weights, a bf16 or FP8_E4M3_B128 cache and page_size a multiple of 64 run
  * on the tensor cores (tcgen05/TMEM/TMA, mla_decode_path() == 1; an FP8 cache
- * is dequantised to bf16 in shared memory before the MMAs); every other valid
+ * is dequantised to fp16 in shared memory before the MMAs); every other valid
  * config runs on CUDA cores. On the tensor-core path the kernels are chained
  * with programmatic dependent launch:
  *   - the first one may start reading W_UK before the kernel that precedes
