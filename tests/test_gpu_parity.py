@@ -126,6 +126,21 @@ def test_decode_all_outputs_small(name, over):
     T.assert_close(got, want, shape.cache_dtype, name)
 
 
+@pytest.mark.parametrize("batch", [12, 4])
+def test_merge_of_many_partials(batch):
+    # one 40,000-token sequence beside 64-token ones: its tiles span most clusters' shares, so the
+    # merge combines dozens of partials in several rounds. With 12 sequences the merge takes four
+    # 4-element chunks per CTA and eight partials per round, with 4 one chunk and sixteen.
+    shape = S.shape_with("dsv2_b16", batch=batch, lengths=(40000,) + (64,) * (batch - 1))
+    inp = S.make_inputs(shape)
+    dc = T.to_device(inp)
+    T.fill_cache(dc)
+    got = T.run_decode(dc)
+    pairs = [(b, i) for b in (0, 1, batch - 1) for i in (0, 1, 63, 64, 127)]
+    want = T.oracle_outputs(inp, pairs)
+    T.assert_close(np.stack([got[b, i] for b, i in pairs]), want, shape.cache_dtype, f"merge b{batch}")
+
+
 def test_decode_matches_explicit_form_too():
     shape = S.shape_with("dsv2_b16", batch=2, lengths=(77, 300))
     inp = S.make_inputs(shape)
