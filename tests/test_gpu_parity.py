@@ -129,8 +129,8 @@ def test_decode_all_outputs_small(name, over):
 @pytest.mark.parametrize("batch", [12, 4])
 def test_merge_of_many_partials(batch):
     # one 40,000-token sequence beside 64-token ones: its tiles span most clusters' shares, so the
-    # merge combines dozens of partials in several rounds. With 12 sequences the merge takes four
-    # 4-element chunks per CTA and eight partials per round, with 4 one chunk and sixteen.
+    # merge combines dozens of partials in several load groups. With 12 sequences the merge takes
+    # four 4-element chunks per CTA and eight partials per group, with 4 one chunk and sixteen.
     shape = S.shape_with("dsv2_b16", batch=batch, lengths=(40000,) + (64,) * (batch - 1))
     inp = S.make_inputs(shape)
     dc = T.to_device(inp)
