@@ -570,9 +570,11 @@ def run_prefill(args, rank, world, local):
 
 # ----------------------------------------------------------------------------- the oracle arm
 
-def oracle_sample(inp, seconds: float, step: int = 0):
+def oracle_sample(inp, seconds: float, step: int = 0, form: str = "absorbed"):
     """Time the fp64 oracle on a bounded sample of one step: the append of every
-    sequence's newest token, then (sequence, head) decodes until the budget is used."""
+    sequence's newest token, then (sequence, head) decodes until the budget is used,
+    in the absorbed form (W_UK folded into the query, the latent as the value) or the
+    explicit one (per-head keys and values up-projected from the latent first)."""
     from oracle import mla_oracle as O
     s = inp.shape
     st = S.draw_step(inp, step)
@@ -592,6 +594,7 @@ def oracle_sample(inp, seconds: float, step: int = 0):
                                  np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta,
                                  inv_freq=inv_freq)
         cache[b] = (c, kr)
+    head = {"absorbed": O.head_absorbed, "explicit": O.head_explicit}[form]
     t0 = time.perf_counter()
     c_new, k_new, _ = O.append_rows(st.c_new.double().numpy(), st.k_new.double().numpy(), inp.lengths - 1,
                                     cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta, inv_freq=inv_freq)
@@ -601,7 +604,7 @@ def oracle_sample(inp, seconds: float, step: int = 0):
             continue
         c = np.concatenate([cache[b][0], c_new[b:b + 1]])
         kr = np.concatenate([cache[b][1], k_new[b:b + 1]])
-        O.head_absorbed(qn[b, i], qr[b, i], w_uk[i], w_uv[i], c, kr, scale)
+        head(qn[b, i], qr[b, i], w_uk[i], w_uv[i], c, kr, scale)
         done += 1
         tok += len(c)
         if time.perf_counter() - t0 > seconds:
@@ -625,11 +628,17 @@ def host_cores():
 
 
 def cpu_baseline(inp, seconds):
+    """The fp64 oracle's absorbed form (the headline CPU number), and beside it the explicit form
+    with half the time budget."""
     v, done, dt = oracle_sample(inp, seconds)
+    ve, done_e, dt_e = oracle_sample(inp, seconds / 2, form="explicit")
     return {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
             "sample": f"{done} (sequence, head) decodes of {inp.shape.name} in the fp64 absorbed form "
                       f"({dt:.1f} s), plus the append of the step's new tokens; tokens/s = cached tokens "
-                      f"visited / n_heads / time; numpy's BLAS pool had {blas_threads()} threads"}
+                      f"visited / n_heads / time; numpy's BLAS pool had {blas_threads()} threads",
+            "explicit": {"value": ve, "unit": UNIT,
+                         "sample": f"{done_e} (sequence, head) decodes in the fp64 explicit form (per-head keys "
+                                   f"and values up-projected from the latent; {dt_e:.1f} s), same accounting"}}
 
 
 def oracle_prefill_sample(inp, seconds: float, step: int = 0):

@@ -38,3 +38,14 @@ def test_committed_traffic_follows_the_source_digest():
     # a kernel with no committed figure, or a workload never captured, reports none
     assert b.committed_traffic("attend_tc", "no_such_workload") is None
     assert b.committed_traffic("no_such_kernel", "long_b4") is None
+
+
+def test_cpu_baseline_times_both_oracle_forms():
+    # the host-core baseline: the fp64 oracle's absorbed form, and beside it the explicit form
+    import mla_synth as S
+    b = _bench()
+    inp = S.make_inputs(S.shape_with("dsv2_b16", batch=2, lengths=(70, 130)))
+    r = b.cpu_baseline(inp, 0.3)
+    assert r["kind"] == "oracle" and r["cores"] == (os.cpu_count() or 1)
+    assert r["value"] > 0 and r["explicit"]["value"] > 0
+    assert "absorbed" in r["sample"] and "explicit" in r["explicit"]["sample"]
