@@ -570,36 +570,45 @@ def run_prefill(args, rank, world, local):
 
 # ----------------------------------------------------------------------------- the oracle arm
 
-def oracle_sample(inp, seconds: float, step: int = 0, form: str = "absorbed"):
+def _sample_order(batch: int, n_heads: int, step: int):
+    rng = np.random.default_rng(step)
+    return [(int(b), int(i)) for b, i in zip(rng.integers(0, batch, 1 << 16), rng.integers(0, n_heads, 1 << 16))]
+
+
+def oracle_prep(inp):
+    """What timed oracle samples start from (not timed: it is resident state, the same for every
+    step): the weights in fp64 and the cache content of up to 64 sequences the samples may touch."""
+    from oracle import mla_oracle as O
+    s = inp.shape
+    inv_freq = O.yarn_inv_freq(s.d_rope, s.rope_theta, s.yarn_factor, s.yarn_alpha, s.yarn_beta, s.yarn_orig_len)
+    cache = {}
+    for b in sorted({b for b, _ in _sample_order(s.batch, s.n_heads, 0)[:64]}):
+        o0, o1 = int(inp.token_offsets[b]), int(inp.token_offsets[b + 1]) - 1
+        c, kr, _ = O.append_rows(inp.c_kv_raw[o0:o1].double().numpy(), inp.k_rope_raw[o0:o1].double().numpy(),
+                                 np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta,
+                                 inv_freq=inv_freq)
+        cache[b] = (c, kr)
+    return {"cache": cache, "inv_freq": inv_freq, "w_uk": inp.w_uk.double().numpy(),
+            "w_uv": inp.w_uv.double().numpy(), "scale": s.scale * O.yarn_logit_factor(s.yarn_factor, s.yarn_mscale)}
+
+
+def oracle_sample(inp, seconds: float, step: int = 0, form: str = "absorbed", prep=None):
     """Time the fp64 oracle on a bounded sample of one step: the append of every
     sequence's newest token, then (sequence, head) decodes until the budget is used,
     in the absorbed form (W_UK folded into the query, the latent as the value) or the
     explicit one (per-head keys and values up-projected from the latent first)."""
     from oracle import mla_oracle as O
     s = inp.shape
-    st = S.draw_step(inp, step)
-    rng = np.random.default_rng(step)
-    w_uk = inp.w_uk.double().numpy()
-    w_uv = inp.w_uv.double().numpy()
+    p = oracle_prep(inp) if prep is None else prep
+    cache, inv_freq, scale, w_uk, w_uv = p["cache"], p["inv_freq"], p["scale"], p["w_uk"], p["w_uv"]
+    st = S.draw_step(inp, step)   # the step's queries and new tokens
     qn, qr = st.q_nope.double().numpy(), st.q_rope.double().numpy()
-    inv_freq = O.yarn_inv_freq(s.d_rope, s.rope_theta, s.yarn_factor, s.yarn_alpha, s.yarn_beta, s.yarn_orig_len)
-    scale = s.scale * O.yarn_logit_factor(s.yarn_factor, s.yarn_mscale)
-    # cache content of the sequences the sample touches (not timed: it is resident state)
-    order = [(int(b), int(i)) for b, i in zip(rng.integers(0, s.batch, 1 << 16), rng.integers(0, s.n_heads, 1 << 16))]
-    seqs = sorted({b for b, _ in order[:64]})
-    cache = {}
-    for b in seqs:
-        o0, o1 = int(inp.token_offsets[b]), int(inp.token_offsets[b + 1]) - 1
-        c, kr, _ = O.append_rows(inp.c_kv_raw[o0:o1].double().numpy(), inp.k_rope_raw[o0:o1].double().numpy(),
-                                 np.arange(o1 - o0), cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta,
-                                 inv_freq=inv_freq)
-        cache[b] = (c, kr)
     head = {"absorbed": O.head_absorbed, "explicit": O.head_explicit}[form]
     t0 = time.perf_counter()
     c_new, k_new, _ = O.append_rows(st.c_new.double().numpy(), st.k_new.double().numpy(), inp.lengths - 1,
                                     cache_dtype=s.cache_dtype, eps=s.eps, theta=s.rope_theta, inv_freq=inv_freq)
     done, tok = 0, 0
-    for b, i in order:
+    for b, i in _sample_order(s.batch, s.n_heads, step):
         if b not in cache:
             continue
         c = np.concatenate([cache[b][0], c_new[b:b + 1]])
@@ -630,8 +639,9 @@ def host_cores():
 def cpu_baseline(inp, seconds):
     """The fp64 oracle's absorbed form (the headline CPU number), and beside it the explicit form
     with half the time budget."""
-    v, done, dt = oracle_sample(inp, seconds)
-    ve, done_e, dt_e = oracle_sample(inp, seconds / 2, form="explicit")
+    prep = oracle_prep(inp)
+    v, done, dt = oracle_sample(inp, seconds, prep=prep)
+    ve, done_e, dt_e = oracle_sample(inp, seconds / 2, form="explicit", prep=prep)
     return {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
             "sample": f"{done} (sequence, head) decodes of {inp.shape.name} in the fp64 absorbed form "
                       f"({dt:.1f} s), plus the append of the step's new tokens; tokens/s = cached tokens "
@@ -700,12 +710,13 @@ def run_reference(args, rank, world):
                                  "sample": f"each step: {per_step:.1f} s of single-head fp64 explicit-form prefills "
                                            f"of one {shape.name} prompt; numpy's BLAS pool had {blas_threads()} threads"},
                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    prep = oracle_prep(inp)   # the resident cache, built once
     for k in range(args.warmup):
-        oracle_sample(inp, min(1.0, args.cpu_seconds / 10), k)
+        oracle_sample(inp, min(1.0, args.cpu_seconds / 10), k, prep=prep)
     vals, secs = [], 0.0
     per_step = max(0.5, args.cpu_seconds / max(1, args.steps))
     for k in range(args.steps):
-        v, done, dt = oracle_sample(inp, per_step, args.warmup + k)
+        v, done, dt = oracle_sample(inp, per_step, args.warmup + k, prep=prep)
         vals.append(v)
         secs += dt
     value = float(np.mean(vals))
